@@ -1,0 +1,396 @@
+#!/usr/bin/env python3
+"""Throughput of the MoE route -> plan -> permute -> combine hot path.
+
+One step = route_topk + plan (2 launches) + permute + combine over one batch
+of a synthetic workload already resident in HBM (experts are the identity:
+the combine reads the permuted buffer back).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config mixtral]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+Multi-GPU runs (torchrun, one rank per GPU) are independent replicas of the
+same workload on every rank (the path has no exchange step on one node's
+logical ranks): value = all ranks' tokens / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "routed tokens/s (route+plan+permute+combine)"
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ---------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, group=None) -> float:
+    """Max over ranks (identity without an initialised process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    backend = dist.get_backend(group)
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
+def barrier(group=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier(group=group)
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def algorithmic_bytes(w, P: int) -> dict:
+    """HBM bytes each kernel must move at minimum (per launch)."""
+    N, E, K, H, R = w.N, w.E, w.K, w.H, w.R
+    NK = N * K
+    return {
+        "route": 4 * N * E + 8 * NK + (4 * E if w.bias else 0),
+        "plan_count": 4 * NK,
+        "plan_scatter": 4 * NK + 4 * NK + 4 * (NK + E * (w.alignment - 1)) + N * R + 4 * NK,
+        "permute": 2 * N * H + 2 * P * H + 4 * NK,
+        "combine": 2 * NK * H + 2 * N * H + 8 * NK,
+    }
+
+
+def source_hash(*names) -> str:
+    h = hashlib.sha1()
+    for n in names:
+        with open(os.path.join(ROOT, "expert_dispatch_planning_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def committed_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel
+    source is unchanged since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[workload][kernel]
+        if e.get("source_sha") != source_hash(*e["sources"]):
+            return None
+        return int(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = open(os.path.join("/tmp", "moe_clocks_%d.csv" % os.getpid()), "w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.out is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.out.flush()
+        self.out.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.read().strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        self.out.close()
+        try:
+            os.remove(self.out.name)
+        except OSError:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_step(w, inp, n_tokens: int):
+    import oracle
+    logits = inp["logits"][:n_tokens]
+    x = inp["x_bits"][:n_tokens]
+    idx, wt = oracle.route_topk(logits, w.K, scoring=w.scoring, renormalize=w.renormalize, bias=inp["bias"],
+                                n_group=w.n_group, topk_group=w.topk_group, routed_scaling=w.routed_scaling)
+    p = oracle.plan(idx, w.E, w.R, w.alignment)
+    perm = oracle.permute(x, p["dst"], p["zero_fill_ranges"], w.K, p["P_cap"])
+    oracle.combine(perm, wt.astype(np.float32), p["dst"])
+
+
+def oracle_sample_tokens(w) -> int:
+    # about 0.5-1 s of single-core work per step on a server core
+    return min(w.N, max(256, int(2.0e8 // (w.K * w.H + 1))))
+
+
+def cpu_baseline(w, inp, min_seconds=10.0, max_steps=40):
+    n = oracle_sample_tokens(w)
+    oracle_step(w, inp, n)   # warm (builds/loads the library)
+    t0 = time.perf_counter()
+    steps = 0
+    while steps < max_steps and (steps < 2 or time.perf_counter() - t0 < min_seconds):
+        oracle_step(w, inp, n)
+        steps += 1
+    dt = time.perf_counter() - t0
+    return {"value": n * steps / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": "%d full oracle steps (route+plan+permute+combine) on the first %d of %d tokens "
+                      "of the %s workload, single-threaded C" % (steps, n, w.N, w.name),
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    inp = workloads.make_inputs(w, seed=0)
+    n = oracle_sample_tokens(w)
+    for _ in range(args.warmup):
+        oracle_step(w, inp, n)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, inp, n)
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_of(w, extra={"sample_tokens": n}),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": "first %d of %d tokens per step, single-threaded C oracle" % (n, w.N)},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w, extra=None):
+    c = {"workload": w.describe(), "N": w.N, "E": w.E, "K": w.K, "R": w.R, "H": w.H,
+         "alignment": w.alignment, "parallelism": "replicas"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import expert_dispatch_planning_gb300 as m
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    m.load()
+
+    inp = workloads.make_inputs(w, seed=0)
+    logits = torch.from_numpy(inp["logits"]).to(dev)
+    bias = None if inp["bias"] is None else torch.from_numpy(inp["bias"]).to(dev)
+    x = torch.from_numpy(inp["x_bits"].view(np.int16)).view(torch.bfloat16).to(dev)
+    rk = dict(scoring=w.scoring, renormalize=w.renormalize, bias=bias, n_group=w.n_group,
+              topk_group=w.topk_group, routed_scaling=w.routed_scaling)
+    stream = torch.cuda.current_stream()
+    p = m.Plan.allocate(w.N, w.E, w.K, w.R, w.alignment, device=dev)
+    idx = torch.empty((w.N, w.K), dtype=torch.int32, device=dev)
+    wts = torch.empty((w.N, w.K), dtype=torch.float32, device=dev)
+    perm = torch.empty((p.P_cap, w.H), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((w.N, w.H), dtype=torch.bfloat16, device=dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        m.route_topk(logits, w.K, topk_idx=idx, topk_w=wts, **rk)
+        if ev:
+            ev[1].record(stream)
+        m.plan(idx, w.E, w.R, w.alignment, out=p)
+        if ev:
+            ev[2].record(stream)
+        m.permute(x, p, out=perm)
+        if ev:
+            ev[3].record(stream)
+        m.combine(perm, wts, p, out=out)
+        if ev:
+            ev[4].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    status = m.get_status(p)
+    if status != 0:
+        raise RuntimeError("device status %d during warm-up" % status)
+    P = int(p.cu_seqlens[-1].item())
+
+    # ---- timed region: K steps, per-stage events on the launching stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[torch.cuda.current_device()]))
+    with clocks:
+        barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    local_ms = start.elapsed_time(stop)
+    ms = reduce_max(local_ms)
+    stage_ms = {k: float(np.mean([e[j].elapsed_time(e[j + 1]) for e in evs]))
+                for j, k in enumerate(["route", "plan", "permute", "combine"])}
+    assert m.get_status(p) == 0
+
+    # ---- end to end through host buffers (pinned), copies inside the region
+    h_logits = torch.from_numpy(inp["logits"]).pin_memory()
+    h_x = torch.from_numpy(inp["x_bits"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_out = torch.empty((w.N, w.H), dtype=torch.bfloat16).pin_memory()
+    d_logits = torch.empty_like(logits)
+    d_x = torch.empty_like(x)
+
+    def e2e_step():
+        d_logits.copy_(h_logits, non_blocking=True)
+        d_x.copy_(h_x, non_blocking=True)
+        m.route_topk(d_logits, w.K, topk_idx=idx, topk_w=wts, **rk)
+        m.plan(idx, w.E, w.R, w.alignment, out=p)
+        m.permute(d_x, p, out=perm)
+        m.combine(perm, wts, p, out=out)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(3, args.steps // 2)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1)) / e_steps
+    barrier()
+
+    if rank != 0:
+        if dist.is_initialized():
+            dist.destroy_process_group()
+        return 0
+
+    cpu = cpu_baseline(w, inp) if ws == 1 and not args.no_cpu_baseline else None
+    ms_step = ms / args.steps
+    value = ws * w.N / (ms_step * 1e-3)
+    ab = algorithmic_bytes(w, P)
+    peak, peak_kind = measured_peaks()
+    dom = "permute" if stage_ms["permute"] >= stage_ms["combine"] else "combine"
+    achieved = ab[dom] / (stage_ms[dom] * 1e-3) / 1e9
+    kernels = {k: {"ms": round(stage_ms[k], 5),
+                   "gbs": round((ab[k] if k in ab else ab["plan_count"] + ab["plan_scatter"])
+                                / (stage_ms[k] * 1e-3) / 1e9, 1)}
+               for k in stage_ms}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_of(w, extra={"P": P, "l2": "inputs larger than L2 (%.0f MB touched per step)"
+                                      % (sum(ab[k] for k in ("permute", "combine")) / 1e6),
+                                      "experts": "identity (combine reads the permuted rows)"}),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "traffic": committed_traffic(dom, w.name),
+                     "algorithmic_bytes": ab[dom]},
+        "kernels": kernels,
+        "route_plan_us": round(1e3 * (stage_ms["route"] + stage_ms["plan"]), 2),
+        "cpu_baseline": cpu,
+        "e2e": {"value": ws * w.N / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h_logits.numel() * 4 + h_x.numel() * 2),
+                "d2h_bytes_per_step": int(h_out.numel() * 2), "ms_per_step": e2e_ms},
+        "gpu_launches": 5 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if dist.is_initialized():
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="mixtral", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    w = workloads.get(args.config)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,73 @@
+// abi.cu -- host-side pieces of the C ABI shared by every entry point:
+// status strings, reading the plan's device status word, launch settings
+// (programmatic dependent launch, SM count) and the bounded-wait test hook.
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+
+#include "moe_common.cuh"
+
+namespace {
+std::atomic<int> g_skip_tile{-1};
+std::atomic<int64_t> g_timeout_ns{1000000000};  // 1 s
+}  // namespace
+
+namespace moe_host {
+
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("MOE_PDL");
+        return v == nullptr || std::strcmp(v, "0") != 0;
+    }();
+    return on;
+}
+
+int num_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    static int cached_dev = -1;
+    static int cached = 0;
+    if (dev != cached_dev) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cached = n;
+        cached_dev = dev;
+    }
+    return cached;
+}
+
+int64_t timeout_ns() { return g_timeout_ns.load(); }
+int skip_tile() { return g_skip_tile.load(); }
+
+}  // namespace moe_host
+
+extern "C" MOE_API const char* moe_status_string(int code) {
+    switch (code) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported combination";
+        case MOE_ERR_CAPACITY: return "buffer too small";
+        case MOE_ERR_CUDA: return "CUDA runtime error";
+        case MOE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case MOE_ERR_DEVICE_INDEX: return "device index out of range";
+        case MOE_ERR_WORKSPACE: return "plan workspace not initialised";
+        default: return "unknown status";
+    }
+}
+
+extern "C" MOE_API int moe_get_status(const MoePlanOut* plan, int32_t* device_status, cudaStream_t stream) {
+    if (plan == nullptr || plan->status == nullptr || device_status == nullptr) return MOE_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+    int32_t host[2] = {0, 0};
+    if (cudaMemcpy(host, plan->status, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemset(plan->status, 0, sizeof(host)) != cudaSuccess) return MOE_ERR_CUDA;
+    *device_status = host[0];
+    return MOE_OK;
+}
+
+extern "C" MOE_API int moe_debug_set_plan_fault(int skip_tile, int64_t timeout_ns) {
+    if (skip_tile < -1 || timeout_ns < 0) return MOE_ERR_INVALID_ARG;
+    g_skip_tile.store(skip_tile);
+    g_timeout_ns.store(timeout_ns > 0 ? timeout_ns : 1000000000);
+    return MOE_OK;
+}

@@ -1,0 +1,584 @@
+// plan.cu -- dispatch plan for one GPU (sm_103a): histogram, aligned
+// offsets, stable slots, per-rank duplicate detection, rank matrices and
+// the dedup structures, in two launches and without any grid barrier.
+//
+// Pairs are cut into tiles of whole tokens.  Inside a tile each warp owns a
+// contiguous run of tokens and walks it in iterations of floor(32/K) tokens,
+// one lane per (token, k) pair, so lanes are in flat-pair order.
+//
+// Launch 1 (plan_count_kernel), one CTA per tile, tile id from a ticket so
+// that a CTA only ever waits on tiles already running:
+//   - per-tile counts of every "column": the E experts, then tokens per rank
+//     (R columns), then (groups, duplicates);  __match_any_sync groups lanes
+//     with the same expert so one leader adds the run length (MoonEP
+//     moonep/planning.py, run_c1 pass A), and groups lanes with the same
+//     (token, rank) for the duplicate test;
+//   - a decoupled look-back per column gives the exclusive prefix over
+//     earlier tiles (the single-pass replacement of MoonEP's grid-wide
+//     per-expert prefix over blocks and of TensorRT-LLM's atomic tile
+//     offsets); flags carry a call epoch so nothing needs clearing, waits
+//     are bounded in time;
+//   - the last tile holds the totals and writes tokens_per_expert, the
+//     alignment-padded cu_seqlens and zero_fill_ranges (MoonEP per-rank
+//     cu_seqlens / zero_fill_ranges; DeepEP notify_dispatch aligned counts)
+//     and the rank arrays (DeepEP notify_dispatch rank prefix).
+// Launch 2 (plan_scatter_kernel), one CTA per tile:
+//   - re-derives each pair's rank among same-expert pairs of its warp run
+//     (match.any + popc, per-warp running counts in shared memory), scans
+//     the runs per expert, and writes the canonical slot
+//     cu[e] + (pairs of e in earlier tiles) + (in earlier runs) + rank;
+//   - dst = slot for the first pair of a token on a rank, -slot-1 for the
+//     later ones (MoonEP duplicate canonicalisation), src_of_slot (MoonEP
+//     src_info), is_token_in_rank, and the dedup structures in (token,
+//     first k) order;
+//   - -1 into the padding rows and unused capacity of src_of_slot.
+#include "moe_common.cuh"
+
+namespace moe {
+
+constexpr int PLAN_THREADS = 512;
+constexpr int PLAN_WARPS = PLAN_THREADS / 32;
+constexpr int PLAN_IPT_MAX = 8;
+constexpr int LOOKBACK_WINDOW = 16;
+constexpr uint32_t ST_AGG = 1u, ST_PRE = 2u, ST_ERR = 3u;
+
+struct WsHeader {
+    uint32_t epoch;   // epoch of the last completed call
+    uint32_t ticket;  // next tile id of the running call
+    uint32_t done;    // CTAs of the running call that finished
+    uint32_t pad[13];
+};
+static_assert(sizeof(WsHeader) == 64, "header size");
+
+struct PlanArgs {
+    const int32_t* topk;
+    MoePlanOut out;
+    WsHeader* hdr;
+    uint64_t* flags;       // [T][C]
+    int32_t* tile_prefix;  // [T][C]
+    int N, E, K, R, epn, alignment;
+    int tpw, ipt, tile_tokens, T, C;
+    int64_t p_cap;
+    int skip_tile;
+    int64_t timeout_ns;
+};
+
+__device__ __forceinline__ uint64_t pack_flag(uint32_t epoch, uint32_t st, uint32_t v) {
+    return (static_cast<uint64_t>(epoch) << 32) | (static_cast<uint64_t>(st) << 30) | (v & 0x3fffffffu);
+}
+
+// Exclusive prefix sum of n values (n <= 4096) in shared memory by one CTA
+// of PLAN_THREADS threads: out[0] = 0, out[i+1] = out[i] + in[i].
+// `in` and `out` may not alias; s_warp holds PLAN_WARPS + 1 ints.
+__device__ void block_exclusive_scan(const int32_t* in, int n, int32_t* out, int32_t* s_warp) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int chunk = (n + PLAN_THREADS - 1) / PLAN_THREADS;
+    const int b = min(n, tid * chunk), e = min(n, b + chunk);
+    int32_t local = 0;
+    for (int i = b; i < e; ++i) local += in[i];
+    int32_t incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t y = __shfl_up_sync(FULL_MASK, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (tid == 0) {
+        int32_t run = 0;
+        for (int w = 0; w < PLAN_WARPS; ++w) {
+            const int32_t v = s_warp[w];
+            s_warp[w] = run;
+            run += v;
+        }
+        s_warp[PLAN_WARPS] = run;
+    }
+    __syncthreads();
+    int32_t run = s_warp[warp] + incl - local;
+    for (int i = b; i < e; ++i) {
+        out[i] = run;
+        run += in[i];
+    }
+    if (tid == 0) out[n] = s_warp[PLAN_WARPS];
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------- launch 1
+__global__ void __launch_bounds__(PLAN_THREADS) plan_count_kernel(const PlanArgs a) {
+    extern __shared__ __align__(16) int32_t s_dyn[];
+    int32_t* s_tot = s_dyn;               // [C]  counts, then totals
+    int32_t* s_tmp = s_dyn + a.C;         // [E + R + 2] scratch for the last tile
+    int32_t* s_scan = s_tmp + a.E + a.R + 2;  // [E + R + 2]
+    __shared__ int32_t s_warp[PLAN_WARPS + 1];
+    __shared__ int s_tile;
+    __shared__ uint32_t s_epoch;
+    __shared__ int s_err;
+
+    pdl_wait();
+    pdl_trigger();
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int E = a.E, K = a.K, R = a.R, C = a.C;
+    if (tid == 0) {
+        s_tile = static_cast<int>(atomicAdd(&a.hdr->ticket, 1u));
+        s_epoch = *reinterpret_cast<volatile uint32_t*>(&a.hdr->epoch) + 1u;
+        s_err = 0;
+    }
+    for (int c = tid; c < C; c += PLAN_THREADS) s_tot[c] = 0;
+    __syncthreads();
+    const int tile = s_tile;
+    const uint32_t epoch = s_epoch;
+    const bool tile_ok = tile >= 0 && tile < a.T;
+    if (!tile_ok && tid == 0) record_error(a.out.status, MOE_ERR_WORKSPACE, tile);
+
+    if (tile_ok) {
+        // ---- per-tile counts
+        const unsigned lt = (1u << lane) - 1u;
+        const int act = a.tpw * K;
+        const int tok_in_iter = lane / K, k = lane - (lane / K) * K;
+        int my_groups = 0, my_dups = 0;
+        for (int i = 0; i < a.ipt; ++i) {
+            const int64_t s = static_cast<int64_t>(tile) * a.tile_tokens +
+                              static_cast<int64_t>(warp * a.ipt + i) * a.tpw + tok_in_iter;
+            bool active = lane < act && s < a.N;
+            int e = E;
+            if (active) {
+                e = __ldg(a.topk + s * K + k);
+                if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
+                    record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(s * K + k));
+                    active = false;
+                    e = E;
+                }
+            }
+            const unsigned peers = __match_any_sync(FULL_MASK, e);
+            if (active && (peers & lt) == 0u) atomicAdd(&s_tot[e], __popc(peers));
+            const int r = active ? e / a.epn : 0;
+            const unsigned key = active ? static_cast<unsigned>(tok_in_iter * 128 + r) : 0xffffffffu;
+            const unsigned pd = __match_any_sync(FULL_MASK, key);
+            const bool prim = active && (pd & lt) == 0u;
+            if (prim) {
+                atomicAdd(&s_tot[E + r], 1);
+                if (__popc(pd) >= 2) ++my_groups;
+            }
+            if (active && !prim) ++my_dups;
+        }
+        my_groups = __reduce_add_sync(FULL_MASK, my_groups);
+        my_dups = __reduce_add_sync(FULL_MASK, my_dups);
+        if (lane == 0) {
+            atomicAdd(&s_tot[E + R], my_groups);
+            atomicAdd(&s_tot[E + R + 1], my_dups);
+        }
+        __syncthreads();
+
+        // ---- decoupled look-back, one thread per column
+        if (tile != a.skip_tile) {
+            for (int c = tid; c < C; c += PLAN_THREADS) {
+                const int32_t local = s_tot[c];
+                uint64_t* mine = a.flags + static_cast<size_t>(tile) * C + c;
+                int32_t excl = 0;
+                bool err = false;
+                if (tile == 0) {
+                    st_relaxed_u64(mine, pack_flag(epoch, ST_PRE, static_cast<uint32_t>(local)));
+                } else {
+                    st_relaxed_u64(mine, pack_flag(epoch, ST_AGG, static_cast<uint32_t>(local)));
+                    int j = tile - 1;
+                    uint64_t t0 = 0;
+                    while (true) {
+                        uint64_t w[LOOKBACK_WINDOW];
+#pragma unroll
+                        for (int q = 0; q < LOOKBACK_WINDOW; ++q)
+                            w[q] = (j - q >= 0) ? ld_relaxed_u64(a.flags + static_cast<size_t>(j - q) * C + c) : 0ull;
+                        int consumed = 0;
+                        bool done = false, stall = false;
+#pragma unroll
+                        for (int q = 0; q < LOOKBACK_WINDOW; ++q) {
+                            if (done || stall) continue;
+                            if (j - q < 0 || static_cast<uint32_t>(w[q] >> 32) != epoch) {
+                                stall = true;
+                                continue;
+                            }
+                            const uint32_t st = static_cast<uint32_t>(w[q] >> 30) & 3u;
+                            if (st == ST_ERR) {
+                                err = true;
+                                done = true;
+                                continue;
+                            }
+                            excl += static_cast<int32_t>(w[q] & 0x3fffffffu);
+                            ++consumed;
+                            if (st == ST_PRE) done = true;
+                        }
+                        if (done) break;
+                        j -= consumed;
+                        if (stall) {
+                            const uint64_t now = globaltimer_ns();
+                            if (t0 == 0) {
+                                t0 = now;
+                            } else if (now - t0 > static_cast<uint64_t>(a.timeout_ns)) {
+                                record_error(a.out.status, MOE_ERR_DEVICE_TIMEOUT, tile);
+                                err = true;
+                                break;
+                            }
+                            __nanosleep(100);
+                        }
+                    }
+                    st_relaxed_u64(mine, err ? pack_flag(epoch, ST_ERR, 0u)
+                                             : pack_flag(epoch, ST_PRE, static_cast<uint32_t>(excl + local)));
+                }
+                if (err) s_err = 1;
+                a.tile_prefix[static_cast<size_t>(tile) * C + c] = excl;
+                s_tot[c] = excl + local;
+            }
+        }
+        __syncthreads();
+
+        // ---- last tile: totals -> aligned offsets and rank arrays
+        if (tile == a.T - 1 && tile != a.skip_tile && s_err == 0) {
+            const int al = a.alignment;
+            for (int e = tid; e < E; e += PLAN_THREADS) {
+                const int32_t c = s_tot[e];
+                s_tmp[e] = c > 0 ? static_cast<int32_t>((static_cast<int64_t>(c) + al - 1) / al * al) : 0;
+                a.out.tokens_per_expert[e] = c;
+            }
+            __syncthreads();
+            block_exclusive_scan(s_tmp, E, s_scan, s_warp);  // s_scan[0..E] = cu
+            for (int e = tid; e <= E; e += PLAN_THREADS) a.out.cu_seqlens[e] = s_scan[e];
+            for (int e = tid; e < E; e += PLAN_THREADS) {
+                const int32_t pad = s_tmp[e] - s_tot[e];
+                a.out.zero_fill_ranges[2 * e] = pad > 0 ? s_scan[e] + s_tot[e] : 0;
+                a.out.zero_fill_ranges[2 * e + 1] = pad > 0 ? pad : 0;
+            }
+            for (int r = tid; r <= R; r += PLAN_THREADS) a.out.rank_slot_offsets[r] = s_scan[r * a.epn];
+            for (int r = tid; r < R; r += PLAN_THREADS) {
+                int32_t pairs = 0;
+                for (int e = r * a.epn; e < (r + 1) * a.epn; ++e) pairs += s_tot[e];
+                a.out.pairs_per_rank[r] = pairs;
+                a.out.tokens_per_rank[r] = s_tot[E + r];
+            }
+            if (tid == 0) {
+                a.out.dup_counts[0] = s_tot[E + R];
+                a.out.dup_counts[1] = s_tot[E + R + 1];
+            }
+            __syncthreads();
+            block_exclusive_scan(s_tot + E, R, s_tmp, s_warp);  // s_tmp[0..R] = rank prefix
+            for (int r = tid; r <= R; r += PLAN_THREADS) a.out.rank_prefix[r] = s_tmp[r];
+        }
+    }
+
+    // ---- completion: the last CTA to finish closes the epoch
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        const uint32_t prev = atomicAdd(&a.hdr->done, 1u);
+        if (prev == gridDim.x - 1) {
+            a.hdr->ticket = 0u;
+            a.hdr->done = 0u;
+            a.hdr->epoch = epoch;
+            __threadfence();
+        }
+    }
+}
+
+// ---------------------------------------------------------------- launch 2
+__global__ void __launch_bounds__(PLAN_THREADS) plan_scatter_kernel(const PlanArgs a) {
+    extern __shared__ __align__(16) int32_t s_dyn[];
+    int32_t* s_wc = s_dyn;                                              // [PLAN_WARPS][E]
+    uint8_t* s_itr = reinterpret_cast<uint8_t*>(s_dyn + PLAN_WARPS * a.E);  // [tile_tokens][R]
+    __shared__ int32_t s_wg[PLAN_WARPS], s_wd[PLAN_WARPS];
+    __shared__ int32_t s_bad;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int E = a.E, K = a.K, R = a.R;
+    const int tile = blockIdx.x;
+    const int64_t tok0 = static_cast<int64_t>(tile) * a.tile_tokens;
+    const int itr_bytes = a.tile_tokens * R;
+
+    for (int i = tid; i < PLAN_WARPS * E; i += PLAN_THREADS) s_wc[i] = 0;
+    for (int i = tid; i < (itr_bytes + 3) / 4; i += PLAN_THREADS) reinterpret_cast<int32_t*>(s_itr)[i] = 0;
+    __syncthreads();
+
+    // ---- phase 1: ranks within the warp run, duplicate bookkeeping.  Reads
+    // only topk_idx, which was complete before launch 1 passed its wait.
+    const unsigned lt = (1u << lane) - 1u;
+    const int act = a.tpw * K;
+    const int tok_in_iter = lane / K, k = lane - (lane / K) * K;
+    const int tok_lane0 = tok_in_iter * K;
+    const unsigned below_tok = (1u << tok_lane0) - 1u;
+    int it_e[PLAN_IPT_MAX], it_rank[PLAN_IPT_MAX], it_a[PLAN_IPT_MAX], it_b[PLAN_IPT_MAX], it_f[PLAN_IPT_MAX];
+    int run_g = 0, run_d = 0;
+#pragma unroll
+    for (int i = 0; i < PLAN_IPT_MAX; ++i) {
+        it_e[i] = -1;
+        if (i >= a.ipt) continue;
+        const int64_t s = tok0 + static_cast<int64_t>(warp * a.ipt + i) * a.tpw + tok_in_iter;
+        bool active = lane < act && s < a.N;
+        int e = E;
+        if (active) {
+            e = __ldg(a.topk + s * K + k);
+            if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
+                active = false;
+                e = E;
+            }
+        }
+        const unsigned peers = __match_any_sync(FULL_MASK, e);
+        const int base = active ? s_wc[warp * E + e] : 0;
+        const int wr = base + __popc(peers & lt);
+        __syncwarp();
+        if (active && (peers & lt) == 0u) s_wc[warp * E + e] = base + __popc(peers);
+        __syncwarp();
+
+        const int r = active ? e / a.epn : 0;
+        const unsigned key = active ? static_cast<unsigned>(tok_in_iter * 128 + r) : 0xffffffffu;
+        const unsigned pd = __match_any_sync(FULL_MASK, key);
+        const bool prim = active && (pd & lt) == 0u;
+        const bool dup = active && !prim;
+        const bool opens = prim && __popc(pd) >= 2;
+        const unsigned gball = __ballot_sync(FULL_MASK, opens);
+        const unsigned dball = __ballot_sync(FULL_MASK, dup);
+        // duplicates of this token ordered by (primary lane, lane)
+        const int my_p = __ffs(pd) - 1;
+        int before = 0;
+        for (int j = 0; j < K; ++j) {
+            const int lj = (tok_lane0 + j) & 31;
+            const int pj = __shfl_sync(FULL_MASK, my_p, lj);
+            const int dj = __shfl_sync(FULL_MASK, dup ? 1 : 0, lj);
+            if (dj && (pj < my_p || (pj == my_p && lj < lane))) ++before;
+        }
+        const int dup_pos = run_d + __popc(dball & below_tok) + before;
+        if (prim) s_itr[(s - tok0) * R + r] = 1;
+        if (active) {
+            it_e[i] = e;
+            it_rank[i] = wr;
+            it_f[i] = (dup ? 1 : 0) | (opens ? 2 : 0) | ((__popc(pd) - 1) << 2);
+            it_a[i] = opens ? run_g + __popc(gball & lt) : dup_pos;
+            it_b[i] = dup_pos;
+        }
+        run_g += __popc(gball);
+        run_d += __popc(dball);
+    }
+    if (lane == 0) {
+        s_wg[warp] = run_g;
+        s_wd[warp] = run_d;
+    }
+
+    // ---- everything below needs launch 1's outputs
+    pdl_wait();
+    pdl_trigger();
+    if (tid == 0) s_bad = ld_volatile_s32(a.out.status) != 0 ? 1 : 0;
+    __syncthreads();
+    if (s_bad) return;
+
+    const int32_t* cu = a.out.cu_seqlens;
+    const int32_t* tp = a.tile_prefix + static_cast<size_t>(tile) * a.C;
+    for (int e = tid; e < E; e += PLAN_THREADS) {
+        int32_t run = __ldg(cu + e) + __ldg(tp + e);
+#pragma unroll
+        for (int w = 0; w < PLAN_WARPS; ++w) {
+            const int32_t v = s_wc[w * E + e];
+            s_wc[w * E + e] = run;
+            run += v;
+        }
+    }
+    if (tid == 0) {
+        int32_t g = __ldg(tp + E + R), d = __ldg(tp + E + R + 1);
+        for (int w = 0; w < PLAN_WARPS; ++w) {
+            const int32_t vg = s_wg[w], vd = s_wd[w];
+            s_wg[w] = g;
+            s_wd[w] = d;
+            g += vg;
+            d += vd;
+        }
+    }
+    __syncthreads();
+
+    // ---- phase 3: slots, dst, provenance, dedup structures
+#pragma unroll
+    for (int i = 0; i < PLAN_IPT_MAX; ++i) {
+        if (it_e[i] < 0) continue;
+        const int e = it_e[i];
+        const int64_t s = tok0 + static_cast<int64_t>(warp * a.ipt + i) * a.tpw + tok_in_iter;
+        const int64_t f = s * K + k;
+        const int32_t slot = s_wc[warp * E + e] + it_rank[i];
+        if (slot < 0 || static_cast<int64_t>(slot) >= a.p_cap) {
+            record_error(a.out.status, MOE_ERR_DEVICE_INDEX, slot);
+            continue;
+        }
+        const bool dup = it_f[i] & 1;
+        a.out.dst[f] = dup ? -slot - 1 : slot;
+        a.out.src_of_slot[slot] = static_cast<int32_t>(f);
+        if (it_f[i] & 2) {
+            const int64_t g = static_cast<int64_t>(s_wg[warp]) + it_a[i];
+            if (g >= static_cast<int64_t>(a.N) * (K / 2)) {
+                record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(g));
+                continue;
+            }
+            int32_t* row = a.out.dup_groups + 3 * g;
+            row[0] = slot;
+            row[1] = s_wd[warp] + it_b[i];
+            row[2] = it_f[i] >> 2;
+        } else if (dup) {
+            const int64_t pos = static_cast<int64_t>(s_wd[warp]) + it_a[i];
+            if (pos >= static_cast<int64_t>(a.N) * (K - 1)) {
+                record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(pos));
+                continue;
+            }
+            a.out.dup_loffs[pos] = slot;
+        }
+    }
+
+    // ---- is_token_in_rank rows of this tile (16-byte stores when aligned)
+    {
+        const int64_t ntok = min(static_cast<int64_t>(a.tile_tokens), static_cast<int64_t>(a.N) - tok0);
+        const int64_t nbytes = ntok * R;
+        uint8_t* g = a.out.is_token_in_rank + tok0 * R;
+        if ((reinterpret_cast<uintptr_t>(g) & 15u) == 0) {
+            const int64_t nvec = nbytes / 16;
+            for (int64_t v = tid; v < nvec; v += PLAN_THREADS)
+                reinterpret_cast<uint4*>(g)[v] = reinterpret_cast<const uint4*>(s_itr)[v];
+            for (int64_t b = nvec * 16 + tid; b < nbytes; b += PLAN_THREADS) g[b] = s_itr[b];
+        } else {
+            for (int64_t b = tid; b < nbytes; b += PLAN_THREADS) g[b] = s_itr[b];
+        }
+    }
+
+    // ---- -1 into padding rows (experts tile, tile+T, ...) and unused rows
+    for (int e = tile; e < E; e += a.T) {
+        const int32_t start = __ldg(a.out.zero_fill_ranges + 2 * e);
+        const int32_t cnt = __ldg(a.out.zero_fill_ranges + 2 * e + 1);
+        for (int j = tid; j < cnt; j += PLAN_THREADS) a.out.src_of_slot[start + j] = -1;
+    }
+    {
+        const int64_t P = __ldg(cu + E);
+        const int64_t rest = a.p_cap - P;
+        const int64_t per = (rest + a.T - 1) / a.T;
+        const int64_t b = P + per * tile, e = min(a.p_cap, b + per);
+        for (int64_t j = b + tid; j < e; j += PLAN_THREADS) a.out.src_of_slot[j] = -1;
+    }
+}
+
+}  // namespace moe
+
+// ---------------------------------------------------------------- host
+namespace {
+
+using moe::PlanArgs;
+
+struct Geom {
+    int tpw, ipt, tile_tokens, T, C;
+};
+
+int env_int(const char* name, int dflt) {
+    const char* v = std::getenv(name);
+    return v ? std::atoi(v) : dflt;
+}
+
+Geom plan_geometry(int N, int E, int K, int R) {
+    Geom g;
+    g.tpw = 32 / K;
+    const int64_t pairs = static_cast<int64_t>(N) * K;
+    const int64_t per_iter = static_cast<int64_t>(moe::PLAN_WARPS) * g.tpw * K;
+    // about one tile per SM of a GB300 (152 SMs); fixed so that the workspace
+    // size is a function of the sizes alone
+    constexpr int64_t kTargetTiles = 152;
+    int64_t ipt = (pairs + per_iter * kTargetTiles - 1) / (per_iter * kTargetTiles);
+    const int forced = env_int("MOE_PLAN_IPT", 0);
+    if (forced > 0) ipt = forced;
+    if (ipt < 1) ipt = 1;
+    if (ipt > moe::PLAN_IPT_MAX) ipt = moe::PLAN_IPT_MAX;
+    while (ipt > 1 && static_cast<int64_t>(moe::PLAN_WARPS) * ipt * g.tpw * R > 65536) --ipt;
+    g.ipt = static_cast<int>(ipt);
+    g.tile_tokens = moe::PLAN_WARPS * g.ipt * g.tpw;
+    g.T = static_cast<int>((static_cast<int64_t>(N) + g.tile_tokens - 1) / g.tile_tokens);
+    g.C = E + R + 2;
+    return g;
+}
+
+size_t ws_bytes(const Geom& g) {
+    size_t b = sizeof(moe::WsHeader);
+    b += sizeof(uint64_t) * static_cast<size_t>(g.T) * g.C;
+    b += sizeof(int32_t) * static_cast<size_t>(g.T) * g.C;
+    return (b + 15) / 16 * 16;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_sizes(int N, int E, int K, int R) {
+    if (N < 1 || E < 1 || E > 1024 || K < 1 || K > 32 || K > E || R < 1 || R > 128 || E % R != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(N) * K >= (int64_t(1) << 30)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" MOE_API int64_t moe_plan_capacity_rows(int N, int E, int K, int alignment) {
+    if (N < 1 || E < 1 || K < 1 || alignment < 1) return -1;
+    return static_cast<int64_t>(N) * K + static_cast<int64_t>(E) * (alignment - 1);
+}
+
+extern "C" MOE_API size_t moe_plan_workspace_size(int N, int E, int K, int R) {
+    if (check_sizes(N, E, K, R) != MOE_OK) return 0;
+    return ws_bytes(plan_geometry(N, E, K, R));
+}
+
+extern "C" MOE_API int moe_plan_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (workspace == nullptr || workspace_bytes < sizeof(moe::WsHeader) || !aligned(workspace, 16))
+        return MOE_ERR_INVALID_ARG;
+    return cudaMemsetAsync(workspace, 0, workspace_bytes, stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, int R, int alignment,
+                                void* workspace, size_t workspace_bytes, const MoePlanOut* out,
+                                cudaStream_t stream) {
+    int rc = check_sizes(N, E, K, R);
+    if (rc != MOE_OK) return rc;
+    if (alignment < 1 || topk_idx == nullptr || workspace == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+    const int64_t p_cap = moe_plan_capacity_rows(N, E, K, alignment);
+    if (p_cap >= (int64_t(1) << 31) - 1) return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {out->tokens_per_expert, out->cu_seqlens, out->zero_fill_ranges, out->pairs_per_rank,
+                          out->tokens_per_rank,   out->rank_prefix, out->rank_slot_offsets, out->dst,
+                          out->src_of_slot,       out->dup_groups,  out->dup_loffs,     out->dup_counts,
+                          out->status,            topk_idx};
+    for (const void* p : ptrs)
+        if (p == nullptr || !aligned(p, 4)) return MOE_ERR_INVALID_ARG;
+    if (out->is_token_in_rank == nullptr || !aligned(workspace, 16)) return MOE_ERR_INVALID_ARG;
+
+    const Geom g = plan_geometry(N, E, K, R);
+    if (workspace_bytes < ws_bytes(g)) return MOE_ERR_CAPACITY;
+
+    PlanArgs a;
+    a.topk = topk_idx;
+    a.out = *out;
+    a.hdr = static_cast<moe::WsHeader*>(workspace);
+    a.flags = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) + sizeof(moe::WsHeader));
+    a.tile_prefix = reinterpret_cast<int32_t*>(a.flags + static_cast<size_t>(g.T) * g.C);
+    a.N = N;
+    a.E = E;
+    a.K = K;
+    a.R = R;
+    a.epn = E / R;
+    a.alignment = alignment;
+    a.tpw = g.tpw;
+    a.ipt = g.ipt;
+    a.tile_tokens = g.tile_tokens;
+    a.T = g.T;
+    a.C = g.C;
+    a.p_cap = p_cap;
+    a.skip_tile = moe_host::skip_tile();
+    a.timeout_ns = moe_host::timeout_ns();
+
+    const size_t smem1 = sizeof(int32_t) * (static_cast<size_t>(g.C) + 2 * (E + R + 2) + 2);
+    const size_t smem2 = sizeof(int32_t) * static_cast<size_t>(moe::PLAN_WARPS) * E +
+                         (static_cast<size_t>(g.tile_tokens) * R + 15) / 16 * 16;
+    static bool attr_done = false;
+    if (!attr_done) {
+        if (cudaFuncSetAttribute(moe::plan_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(moe::plan_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) !=
+                cudaSuccess)
+            return MOE_ERR_CUDA;
+        attr_done = true;
+    }
+    rc = moe_host::launch(moe::plan_count_kernel, dim3(g.T), dim3(moe::PLAN_THREADS), smem1, stream, a);
+    if (rc != MOE_OK) return rc;
+    return moe_host::launch(moe::plan_scatter_kernel, dim3(g.T), dim3(moe::PLAN_THREADS), smem2, stream, a);
+}

@@ -1,0 +1,221 @@
+/*
+ * moe_dispatch.h -- C ABI of the GB300 (sm_103a) Mixture-of-Experts routing
+ * and dispatch-planning library.
+ *
+ * One GPU, one CUDA stream per call.  "Ranks" are logical partitions of the
+ * experts computed on this GPU: rank r owns experts [r*E/R, (r+1)*E/R).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers marked (device) point to device memory owned by the caller;
+ *     the library allocates nothing and keeps no pointer after a call.
+ *   - Buffers must not alias one another unless a function says so.
+ *   - bf16 tensors are passed as their 16-bit patterns (uint16_t).
+ *   - A call validates its arguments on the host, enqueues its kernels on
+ *     `stream` and returns without synchronising.  Arguments are checked
+ *     before any CUDA call, so an invalid call has no effect.
+ *   - Return value: MOE_OK or one of the MOE_ERR_* codes below.  Errors that
+ *     only the device can see (an expert id outside [0, E), a bounded wait
+ *     that ran out) are recorded in the plan's device status word and read
+ *     with moe_get_status().
+ *   - Flat pair index f = s*K + k for token s and its k-th expert.
+ *
+ * Sources (page title and section):
+ *   MoonEP moonep/planning.py -- PlanningKernel (histogram, per-expert
+ *     prefix over blocks, stable scatter, per-rank cu_seqlens and
+ *     zero_fill_ranges, dst, duplicate canonicalisation, src_info), the
+ *     MoonEPCommPlan record, allocate_planning_outputs / launch_planning
+ *     (caller-allocated outputs written in place), _check_dedup_encoding_bounds.
+ *   TensorRT-LLM trtllmGenKernels/blockScaleMoe/RoutingKernel.cuh --
+ *     calcSoftmax, sigmoid_accurate, routingIndicesHistogramKernel /
+ *     routingIndicesOffsetsKernel (expanded -> permuted index).
+ *   DeepEP csrc/kernels/intranode.cu -- notify_dispatch (rank prefix
+ *     matrix, aligned per-expert receive counts, is_token_in_rank),
+ *     dispatch (hidden-row copy), combine (fp32 accumulation, bf16 store),
+ *     host-side argument assertions.
+ */
+#ifndef MOE_DISPATCH_H
+#define MOE_DISPATCH_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* ---------------------------------------------------------------- status */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG 1      /* a size, pointer or option is out of range      */
+#define MOE_ERR_UNSUPPORTED 2      /* a valid combination this library does not run  */
+#define MOE_ERR_CAPACITY 3         /* a caller buffer is smaller than required       */
+#define MOE_ERR_CUDA 4             /* a CUDA runtime call or kernel launch failed    */
+#define MOE_ERR_DEVICE_TIMEOUT 5   /* (device) a bounded wait ran out                */
+#define MOE_ERR_DEVICE_INDEX 6     /* (device) an expert id or slot out of range     */
+#define MOE_ERR_WORKSPACE 7        /* (device) plan workspace not initialised        */
+
+#define MOE_SCORING_SOFTMAX 0
+#define MOE_SCORING_SIGMOID 1
+
+/* Human-readable name of a status code (static string). */
+MOE_API const char* moe_status_string(int code);
+
+/* ---------------------------------------------------------------- router */
+/*
+ * Router top-K (TensorRT-LLM calcSoftmax / sigmoid_accurate; tie rule of
+ * MoonEP warp_argmax_min_idx).
+ *
+ *   logits        (device) float32[N][E], row-major, 16-byte aligned.
+ *   bias          (device) float32[E] correction bias or NULL; sigmoid only.
+ *   scoring       MOE_SCORING_SOFTMAX: the selection key is the logit;
+ *                 MOE_SCORING_SIGMOID: key = sigmoid(logit) + bias, with
+ *                 sigmoid evaluated by one fixed fp32 sequence
+ *                 (1/(1+e^-x) for x >= 0, e^x/(1+e^x) otherwise; e^t by
+ *                 Cody-Waite reduction with ln2 split 16+24 bits and the
+ *                 degree-7 Taylor polynomial in Horner form with fused
+ *                 multiply-adds; scaling by two exact powers of two).
+ *   n_group,      group-limited selection (sigmoid only): experts form
+ *   topk_group    n_group contiguous groups (n_group <= 32, E % n_group
+ *                 == 0); a group scores the fp32 sum of its two largest
+ *                 keys; the topk_group best groups are kept and top-K runs
+ *                 over their experts.  n_group = 1 disables it.
+ *   K             1 <= K <= 32, K <= E (and <= topk_group*E/n_group).
+ *   renormalize   softmax: weights are the softmax over the K selected
+ *                 logits (1) or over all E (0).  sigmoid: w_k = s_k / sum
+ *                 of the K selected scores (1) or s_k (0).  Scores are
+ *                 unbiased.  All weights are multiplied by routed_scaling.
+ *   topk_idx      (device) int32[N][K] out: descending key, equal keys in
+ *                 ascending expert index.
+ *   topk_w        (device) float32[N][K] out, within 1e-6 relative of the
+ *                 exact value.
+ * 1 <= N, 1 <= E <= 1024, E % 4 == 0 for the vector path (any E works).
+ * NaN logits are outside the contract (their position in the order is
+ * unspecified).
+ */
+MOE_API int moe_route_topk(const float* logits, const float* bias, int N, int E, int K,
+                           int scoring, int renormalize, int n_group, int topk_group,
+                           float routed_scaling, int32_t* topk_idx, float* topk_w,
+                           cudaStream_t stream);
+
+/* ---------------------------------------------------------------- plan */
+/*
+ * Caller-owned plan outputs (MoonEP MoonEPCommPlan, DeepEP notify_dispatch
+ * outputs, in their single-GPU form).  Every pointer is device memory,
+ * 4-byte aligned (is_token_in_rank and dst 16-byte aligned).  P denotes the
+ * padded row total cu_seqlens[E]; P_cap = moe_plan_capacity_rows(...).
+ */
+typedef struct MoePlanOut {
+    int32_t* tokens_per_expert;  /* [E]     pairs routed to each expert                    */
+    int32_t* cu_seqlens;         /* [E+1]   0, then running sum of padded counts; padded
+                                    = round_up(count, alignment) if count > 0 else 0      */
+    int32_t* zero_fill_ranges;   /* [E][2]  (cu[e]+count, padded-count) if positive, else
+                                    (0, 0)                                                */
+    int32_t* pairs_per_rank;     /* [R]     pairs routed to each rank's experts           */
+    int32_t* tokens_per_rank;    /* [R]     tokens with at least one pair on the rank     */
+    int32_t* rank_prefix;        /* [R+1]   exclusive prefix of tokens_per_rank           */
+    int32_t* rank_slot_offsets;  /* [R+1]   cu_seqlens[r*E/R]: first row of each rank     */
+    uint8_t* is_token_in_rank;   /* [N][R]  1 if token s has a pair on rank r            */
+    int32_t* dst;                /* [N][K]  raw slot (row of the permuted buffer) of the
+                                    pair; -slot-1 when an earlier k of the same token
+                                    already reached that rank (a duplicate)               */
+    int32_t* src_of_slot;        /* [P_cap] flat pair index f of each row, -1 for padding
+                                    and unused rows                                       */
+    int32_t* dup_groups;         /* [N*(K/2)][3] (primary slot, dup_begin, dup_count) for
+                                    each (token, rank) holding >= 2 pairs, in (token,
+                                    first k) order                                        */
+    int32_t* dup_loffs;          /* [N*(K-1)] duplicate slots, group after group, k order */
+    int32_t* dup_counts;         /* [2]     (number of groups, number of duplicates)     */
+    int32_t* status;             /* [4]     device status: [0] first error code (0 = ok),
+                                    [1] detail.  Zero it before first use; read and
+                                    cleared by moe_get_status.                            */
+} MoePlanOut;
+
+/* Rows the permuted buffer needs: N*K + E*(alignment-1).  -1 on bad input. */
+MOE_API int64_t moe_plan_capacity_rows(int N, int E, int K, int alignment);
+
+/* Bytes of device workspace moe_plan needs for these sizes (0 on bad input). */
+MOE_API size_t moe_plan_workspace_size(int N, int E, int K, int R);
+
+/*
+ * Prepare a workspace for its first use (enqueues a memset on `stream`).
+ * A workspace carries a call counter between calls, so it must be
+ * initialised once after allocation; afterwards any number of moe_plan
+ * calls (of any sizes it fits) may use it, one at a time.
+ */
+MOE_API int moe_plan_workspace_init(void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream);
+
+/*
+ * Dispatch plan (MoonEP PlanningKernel; TensorRT-LLM histogram / offsets
+ * kernels; DeepEP notify_dispatch).
+ *
+ *   topk_idx   (device) int32[N][K] expert ids in [0, E).
+ *   R          logical ranks, E % R == 0, R <= 128 (MoonEP's rank-bitset
+ *              bound); alignment >= 1 rows per expert.
+ *   workspace  (device) >= moe_plan_workspace_size(N, E, K, R) bytes,
+ *              16-byte aligned, initialised once (moe_plan_workspace_init).
+ *              Two plans in flight at once must not share a workspace.
+ *   out        host struct of device pointers (see MoePlanOut).
+ *
+ * Slots are canonical: within each expert, pairs keep ascending flat index
+ * (MoonEP's stable scatter order), so the plan is a pure function of
+ * topk_idx.  Checked here: N >= 1, 1 <= K <= 32, K <= E <= 1024,
+ * E % R == 0, R <= 128, N*K < 2^30, P_cap < 2^31.
+ */
+MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, int R, int alignment,
+                     void* workspace, size_t workspace_bytes, const MoePlanOut* out,
+                     cudaStream_t stream);
+
+/* ---------------------------------------------------------------- rows */
+/*
+ * Permute (DeepEP dispatch's hidden-row copy, MoonEP dst / zero_fill_ranges):
+ *   permuted[raw slot(f)] = x[f / K] for every pair, primaries and
+ *   duplicates alike; rows inside the zero-fill ranges are written +0.0;
+ *   rows at or beyond cu_seqlens[E] are left untouched.
+ *   x         (device) bf16[N][H], 16-byte aligned; H % 8 == 0.
+ *   permuted  (device) bf16[P_cap][H], 16-byte aligned, must not alias x.
+ *   plan      the plan built by moe_plan for the same N, E, K, alignment
+ *             (uses dst, zero_fill_ranges, status).
+ */
+MOE_API int moe_permute(const uint16_t* x, int N, int H, int K, int E, int alignment,
+                        const MoePlanOut* plan, uint16_t* permuted, cudaStream_t stream);
+
+/*
+ * Weighted combine (DeepEP combine's fp32 accumulation and bf16 store):
+ *   out[s][h] = bf16_rne(acc), acc = 0, then for k = 0..K-1
+ *       acc = fmaf(topk_w[s][k], float(y[raw slot(s,k)][h]), acc).
+ *   y       (device) bf16[P_cap][H] expert outputs in permuted order.
+ *   topk_w  (device) float32[N][K].
+ *   out     (device) bf16[N][H]; must not alias y.
+ *   plan    uses dst and status.
+ */
+MOE_API int moe_combine(const uint16_t* y, const float* topk_w, int N, int K, int H, int E,
+                        int alignment, const MoePlanOut* plan, uint16_t* out,
+                        cudaStream_t stream);
+
+/* ---------------------------------------------------------------- status */
+/*
+ * Synchronise `stream`, copy the plan's device status to *device_status
+ * (MOE_OK or a MOE_ERR_DEVICE_* / MOE_ERR_WORKSPACE code) and clear it.
+ * Returns MOE_ERR_CUDA if the synchronisation or copy fails.
+ */
+MOE_API int moe_get_status(const MoePlanOut* plan, int32_t* device_status, cudaStream_t stream);
+
+/*
+ * Test hook for the bounded-wait path: while skip_tile >= 0, the planning
+ * kernel's tile `skip_tile` never publishes its counts, so later tiles wait
+ * until `timeout_ns` runs out and report MOE_ERR_DEVICE_TIMEOUT.  Pass
+ * (-1, 0) to restore the defaults (no skipped tile, 1 s limit).
+ */
+MOE_API int moe_debug_set_plan_fault(int skip_tile, int64_t timeout_ns);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_DISPATCH_H */

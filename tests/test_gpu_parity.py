@@ -1,0 +1,317 @@
+"""GPU parity: every step of the CUDA path against the CPU oracle.
+
+Each stage is fed the same seeded inputs as the oracle (the plan gets the
+oracle's routing, the combine the oracle's weights rounded to fp32), so each
+comparison isolates one kernel.  Bars: bit-exact for indices, plans and
+permuted rows; router weights within 1e-6 relative; the combine bit-exact
+(both sides run the same fp32 fused multiply-add sequence; the stated
+tolerance 1e-2 absolute is asserted as well).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from plan_checks import check_plan_invariants
+
+pytestmark = pytest.mark.gpu
+
+PLAN_KEYS = ["tokens_per_expert", "cu_seqlens", "zero_fill_ranges", "dst", "src_of_slot",
+             "is_token_in_rank", "tokens_per_rank", "pairs_per_rank", "rank_prefix",
+             "rank_slot_offsets", "dup_groups", "dup_loffs", "dup_counts"]
+
+
+@pytest.fixture(scope="module")
+def m():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import expert_dispatch_planning_gb300 as mod
+    mod.load()
+    return mod
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def to_bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev())
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def assert_plan_equal(got, want):
+    for k in PLAN_KEYS:
+        g, w = np.asarray(got[k]), np.asarray(want[k])
+        assert g.shape == w.shape and np.array_equal(g, w), "plan field %s differs" % k
+
+
+def route_both(m, logits, K, bias=None, **kw):
+    lg = torch.from_numpy(logits).to(dev())
+    b = None if bias is None else torch.from_numpy(bias).to(dev())
+    idx, w = m.route_topk(lg, K, bias=b, **kw)
+    o_idx, o_w = oracle.route_topk(logits, K, bias=bias, **kw)
+    return idx.cpu().numpy(), w.cpu().numpy(), o_idx, o_w
+
+
+def check_route(m, logits, K, bias=None, **kw):
+    idx, w, o_idx, o_w = route_both(m, logits, K, bias, **kw)
+    assert np.array_equal(idx, o_idx), "first mismatch at row %d" % int(np.argwhere((idx != o_idx).any(1))[0][0])
+    rel = np.abs(w.astype(np.float64) - o_w) / np.maximum(np.abs(o_w), 1e-300)
+    assert rel.max() <= 1e-6, rel.max()
+    return o_idx, o_w
+
+
+def route_kwargs(w):
+    return dict(scoring=w.scoring, renormalize=w.renormalize, n_group=w.n_group,
+                topk_group=w.topk_group, routed_scaling=w.routed_scaling)
+
+
+# ---------------------------------------------------------------- router
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "qwen3", "dsv3", "large"])
+def test_route_configs(m, name):
+    w = workloads.get(name)
+    inp = workloads.make_inputs(w, seed=0, with_x=False)
+    check_route(m, inp["logits"], w.K, inp["bias"], **route_kwargs(w))
+
+
+@pytest.mark.parametrize("E,K,scoring,renorm,ng,tg", [
+    (3, 2, 0, 1, 1, 1), (5, 5, 0, 0, 1, 1), (8, 1, 0, 1, 1, 1), (13, 4, 1, 1, 1, 1),
+    (16, 3, 0, 0, 1, 1), (32, 8, 1, 0, 1, 1), (64, 6, 0, 1, 1, 1), (100, 7, 1, 1, 4, 2),
+    (128, 16, 0, 1, 1, 1), (160, 8, 1, 1, 8, 3), (256, 32, 0, 1, 1, 1), (512, 8, 1, 1, 16, 4),
+    (1024, 8, 0, 0, 1, 1), (1024, 12, 1, 1, 32, 4), (48, 48, 0, 1, 1, 1), (12, 4, 1, 1, 12, 4)])
+def test_route_shapes(m, E, K, scoring, renorm, ng, tg):
+    rng = np.random.default_rng(E * 131 + K)
+    N = 777
+    logits = rng.standard_normal((N, E), dtype=np.float32) * 3
+    # force ties and signed zeros on some rows
+    logits[::7] = np.round(logits[::7])
+    logits[::11, : E // 2] = -0.0
+    bias = rng.uniform(-0.1, 0.1, E).astype(np.float32) if scoring == 1 else None
+    check_route(m, logits, K, bias, scoring=scoring, renormalize=bool(renorm), n_group=ng,
+                topk_group=tg, routed_scaling=1.7)
+
+
+def test_route_extreme_logits(m):
+    rng = np.random.default_rng(5)
+    logits = rng.standard_normal((300, 64), dtype=np.float32) * 60   # sigmoid tails, subnormals
+    logits[0] = 0.0
+    logits[1] = 200.0
+    logits[2] = -200.0
+    check_route(m, logits, 8, rng.uniform(-0.1, 0.1, 64).astype(np.float32), scoring=1,
+                renormalize=True, n_group=8, topk_group=2, routed_scaling=2.5)
+    check_route(m, logits / 10, 8, scoring=0, renormalize=False)
+
+
+# ---------------------------------------------------------------- plan
+def plan_both(m, topk, E, R, a, out=None):
+    p = m.plan(torch.from_numpy(topk).to(dev()), E, R, a, out=out)
+    got = p.to_host()
+    assert m.get_status(p) == 0
+    want = oracle.plan(topk, E, R, a)
+    return p, got, want
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "qwen3", "dsv3", "large"])
+def test_plan_configs(m, name):
+    w = workloads.get(name)
+    inp = workloads.make_inputs(w, seed=0, with_x=False)
+    o_idx, _ = oracle.route_topk(inp["logits"], w.K, bias=inp["bias"], **route_kwargs(w))
+    _, got, want = plan_both(m, o_idx, w.E, w.R, w.alignment)
+    assert_plan_equal(got, want)
+    if name != "large":
+        check_plan_invariants(got, o_idx, w.E, w.R, w.alignment)
+
+
+@pytest.mark.parametrize("N,E,K,R,a,mode", [
+    (1, 8, 2, 2, 8, "rand"), (1, 256, 8, 64, 128, "rand"), (7, 4, 4, 4, 1, "rand"),
+    (333, 16, 1, 1, 4, "rand"), (1000, 8, 8, 8, 3, "rand"), (4097, 64, 3, 16, 16, "rand"),
+    (5000, 32, 6, 32, 7, "rand"), (2500, 128, 16, 8, 64, "rand"), (700, 64, 32, 2, 2, "rand"),
+    (9000, 8, 2, 4, 16, "hot"), (3000, 1024, 8, 128, 128, "rand"), (2049, 24, 5, 3, 9, "dups"),
+    (600, 16, 4, 4, 5, "one"), (12345, 256, 8, 64, 128, "rand"), (20000, 96, 1, 96, 32, "rand")])
+def test_plan_shapes(m, N, E, K, R, a, mode):
+    rng = np.random.default_rng(N + E + K)
+    if mode == "one":      # every pair on expert 3: empty experts, one full
+        topk = np.full((N, K), 3, np.int32)
+        topk[:, 1:] = (3 + np.arange(1, K)) % E
+    elif mode == "dups":   # repeated ids inside a token
+        topk = rng.integers(0, E, size=(N, K)).astype(np.int32)
+    else:
+        topk = workloads.random_topk(rng, N, E, K, hot=0.7 if mode == "hot" else 0.0)
+    _, got, want = plan_both(m, topk, E, R, a)
+    assert_plan_equal(got, want)
+    check_plan_invariants(got, topk, E, R, a)
+
+
+def test_plan_workspace_reuse_across_calls_and_sizes(m):
+    rng = np.random.default_rng(9)
+    E, R, a = 64, 8, 16
+    big = m.Plan.allocate(6000, E, 8, R, a)
+    ws = big.workspace
+    for it in range(6):
+        N = [6000, 100, 5999, 1, 3000, 6000][it]
+        topk = workloads.random_topk(rng, N, E, 8)
+        p = m.Plan.allocate(N, E, 8, R, a)
+        p.workspace = ws          # one workspace, calls of different sizes in sequence
+        _, got, want = plan_both(m, topk, E, R, a, out=p)
+        assert_plan_equal(got, want)
+
+
+def test_plan_bad_expert_id_reports_device_index(m):
+    topk = np.zeros((64, 2), np.int32)
+    topk[10, 1] = 8
+    p = m.plan(torch.from_numpy(topk).to(dev()), 8, 2, 4)
+    assert m.get_status(p) == 6
+
+
+def test_plan_uninitialised_workspace_reports_error(m):
+    topk = workloads.random_topk(np.random.default_rng(3), 4000, 16, 4)
+    t = torch.from_numpy(topk).to(dev())
+    p = m.Plan.allocate(4000, 16, 4, 4, 8)
+    p.workspace.fill_(0xFF)
+    m.plan(t, 16, 4, 8, out=p)
+    assert m.get_status(p) == 7
+    from expert_dispatch_planning_gb300 import _lib
+    _lib.check("init", _lib.load().moe_plan_workspace_init(
+        p.workspace.data_ptr(), p.workspace.numel(), torch.cuda.current_stream().cuda_stream))
+    m.plan(t, 16, 4, 8, out=p)
+    assert m.get_status(p) == 0
+    assert_plan_equal(p.to_host(), oracle.plan(topk, 16, 4, 8))
+
+
+def test_plan_bounded_wait_reports_timeout_and_recovers(m):
+    N, E, K, R, a = 20000, 64, 8, 8, 16     # several tiles
+    topk = workloads.random_topk(np.random.default_rng(4), N, E, K)
+    t = torch.from_numpy(topk).to(dev())
+    p = m.Plan.allocate(N, E, K, R, a)
+    x = torch.zeros((N, 64), dtype=torch.bfloat16, device=dev())
+    sentinel = torch.full((p.P_cap, 64), 7.0, dtype=torch.bfloat16, device=dev())
+    try:
+        m.set_plan_fault(skip_tile=0, timeout_ns=20_000_000)   # tile 0 never publishes
+        m.plan(t, E, R, a, out=p)
+        m.permute(x, p, out=sentinel)                           # must not move rows by a failed plan
+        torch.cuda.synchronize()
+    finally:
+        m.set_plan_fault(-1, 0)
+    assert m.get_status(p) == 5
+    assert bool((sentinel == 7.0).all())
+    m.plan(t, E, R, a, out=p)                                   # the workspace is usable again
+    assert m.get_status(p) == 0
+    assert_plan_equal(p.to_host(), oracle.plan(topk, E, R, a))
+
+
+# ---------------------------------------------------------------- permute / combine
+def rows_case(m, name, N=None):
+    w = workloads.get(name)
+    inp = workloads.make_inputs(w, seed=0, N=N)
+    o_idx, o_w = oracle.route_topk(inp["logits"], w.K, bias=inp["bias"], **route_kwargs(w))
+    p = m.plan(torch.from_numpy(o_idx).to(dev()), w.E, w.R, w.alignment)
+    want = oracle.plan(o_idx, w.E, w.R, w.alignment)
+    assert_plan_equal(p.to_host(), want)
+    return w, inp, o_idx, o_w, p, want
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "qwen3", "dsv3"])
+def test_permute_combine_configs(m, name):
+    w, inp, o_idx, o_w, p, want = rows_case(m, name)
+    x = to_bf16(inp["x_bits"])
+    sentinel = torch.full((p.P_cap, w.H), -3.0, dtype=torch.bfloat16, device=dev())
+    perm = m.permute(x, p, out=sentinel)
+    o_perm = oracle.permute(inp["x_bits"], want["dst"], want["zero_fill_ranges"], w.K, want["P_cap"],
+                            fill=np.full((want["P_cap"], w.H), bits(torch.tensor([-3.0], dtype=torch.bfloat16))[0],
+                                         np.uint16))
+    assert np.array_equal(bits(perm), o_perm)
+    # combine over arbitrary expert outputs y with the oracle's weights in fp32
+    rng = np.random.default_rng(1)
+    y_bits = workloads.make_x_bits(rng, want["P_cap"], w.H)
+    w32 = o_w.astype(np.float32)
+    out = m.combine(to_bf16(y_bits), torch.from_numpy(w32).to(dev()), p)
+    o_out = oracle.combine(y_bits, w32, want["dst"])
+    got = bits(out)
+    assert np.array_equal(got, o_out)
+    diff = np.abs(torch.from_numpy(got.view(np.int16)).view(torch.bfloat16).float().numpy()
+                  - torch.from_numpy(o_out.view(np.int16)).view(torch.bfloat16).float().numpy())
+    assert diff.max() <= 1e-2
+    assert m.get_status(p) == 0
+
+
+def test_permute_combine_large_sampled(m):
+    """Full-size large config in the benchmark's launch configuration; rows
+    checked by properties on the device and sampled tokens against the oracle."""
+    w, inp, o_idx, o_w, p, want = rows_case(m, "large")
+    x = to_bf16(inp["x_bits"])
+    perm = torch.empty((p.P_cap, w.H), dtype=torch.bfloat16, device=dev())
+    perm[want["P"]:] = 5.0
+    m.permute(x, p, out=perm)
+    # every pair's row equals its token row (checked on the device, in chunks)
+    raw = np.where(want["dst"] >= 0, want["dst"], -want["dst"] - 1).astype(np.int64)
+    raw_t = torch.from_numpy(raw).to(dev())
+    for s0 in range(0, w.N, 4096):
+        rows = perm.index_select(0, raw_t[s0:s0 + 4096].reshape(-1)).view(-1, w.K, w.H)
+        assert torch.equal(rows, x[s0:s0 + 4096].unsqueeze(1).expand_as(rows))
+    pads = [np.arange(st, st + c) for st, c in want["zero_fill_ranges"] if c > 0]
+    pads = torch.from_numpy(np.concatenate(pads)).to(dev())
+    assert bool((perm.index_select(0, pads).view(torch.int16) == 0).all())
+    assert bool((perm[want["P"]:] == 5.0).all())
+    # combine: sampled tokens against the oracle, computed one by one
+    w32 = o_w.astype(np.float32)
+    out = m.combine(perm, torch.from_numpy(w32).to(dev()), p)
+    toks = np.random.default_rng(2).choice(w.N, 256, replace=False)
+    ridx = torch.from_numpy(np.unique(raw[toks].ravel())).to(dev())
+    y_rows = bits(perm.index_select(0, ridx))
+    remap = {int(r): i for i, r in enumerate(ridx.cpu().numpy())}
+    local_dst = np.vectorize(lambda r: remap[int(r)])(raw[toks]).astype(np.int32)
+    o_out = oracle.combine(y_rows, w32[toks], local_dst)
+    assert np.array_equal(bits(out)[toks], o_out)
+    assert m.get_status(p) == 0
+
+
+@pytest.mark.parametrize("N,E,K,R,H,a", [(1, 8, 2, 2, 8, 4), (37, 8, 3, 4, 24, 1), (500, 16, 5, 4, 136, 8),
+                                          (1000, 64, 7, 8, 72, 16), (300, 32, 16, 8, 512, 3),
+                                          (129, 64, 32, 4, 64, 2), (2000, 8, 1, 8, 1024, 64)])
+def test_permute_combine_shapes(m, N, E, K, R, H, a):
+    rng = np.random.default_rng(N * 7 + K)
+    topk = workloads.random_topk(rng, N, E, K)
+    p = m.plan(torch.from_numpy(topk).to(dev()), E, R, a)
+    want = oracle.plan(topk, E, R, a)
+    x_bits = workloads.make_x_bits(rng, N, H)
+    perm = torch.full((want["P_cap"], H), 9.0, dtype=torch.bfloat16, device=dev())
+    m.permute(to_bf16(x_bits), p, out=perm)
+    fill = np.full((want["P_cap"], H), bits(torch.tensor([9.0], dtype=torch.bfloat16))[0], np.uint16)
+    assert np.array_equal(bits(perm), oracle.permute(x_bits, want["dst"], want["zero_fill_ranges"], K,
+                                                     want["P_cap"], fill=fill))
+    wts = rng.random((N, K)).astype(np.float32)
+    y_bits = workloads.make_x_bits(rng, want["P_cap"], H)
+    out = m.combine(to_bf16(y_bits), torch.from_numpy(wts).to(dev()), p)
+    assert np.array_equal(bits(out), oracle.combine(y_bits, wts, want["dst"]))
+    assert m.get_status(p) == 0
+
+
+# ---------------------------------------------------------------- end to end
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "dsv3"])
+def test_end_to_end(m, name):
+    """GPU chain route->plan->permute->combine (identity experts) against the
+    oracle chain; weights differ within 1e-6 so the bf16 output may differ by
+    one rounding step where the fp32 sum sits on a rounding boundary."""
+    w = workloads.get(name)
+    inp = workloads.make_inputs(w, seed=0)
+    lg = torch.from_numpy(inp["logits"]).to(dev())
+    b = None if inp["bias"] is None else torch.from_numpy(inp["bias"]).to(dev())
+    x = to_bf16(inp["x_bits"])
+    idx, wts = m.route_topk(lg, w.K, bias=b, **route_kwargs(w))
+    p = m.plan(idx, w.E, w.R, w.alignment)
+    perm = m.permute(x, p)
+    out = m.combine(perm, wts, p)
+    assert m.get_status(p) == 0
+    o_idx, o_w = oracle.route_topk(inp["logits"], w.K, bias=inp["bias"], **route_kwargs(w))
+    op = oracle.plan(o_idx, w.E, w.R, w.alignment)
+    o_perm = oracle.permute(inp["x_bits"], op["dst"], op["zero_fill_ranges"], w.K, op["P_cap"])
+    o_out = oracle.combine(o_perm, o_w.astype(np.float32), op["dst"])
+    g = torch.from_numpy(bits(out).view(np.int16)).view(torch.bfloat16).double().numpy()
+    o = torch.from_numpy(o_out.view(np.int16)).view(torch.bfloat16).double().numpy()
+    ulp = np.maximum(np.abs(o), 2.0 ** -126) * 2.0 ** -7
+    assert np.all(np.abs(g - o) <= np.maximum(1e-2, ulp * 1.0001))
+    assert np.mean(g != o) < 1e-3
