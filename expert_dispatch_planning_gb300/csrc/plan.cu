@@ -63,8 +63,13 @@ struct PlanArgs {
     int64_t timeout_ns;
 };
 
+// A flag word: tag in the high half, state and value in the low half.  The
+// tag is the call epoch with bit 31 set: counts and prefixes left in the
+// workspace by calls of other sizes are below 2^30, so no leftover word can
+// carry the tag of the running call.
+__device__ __forceinline__ uint32_t flag_tag(uint32_t epoch) { return epoch | 0x80000000u; }
 __device__ __forceinline__ uint64_t pack_flag(uint32_t epoch, uint32_t st, uint32_t v) {
-    return (static_cast<uint64_t>(epoch) << 32) | (static_cast<uint64_t>(st) << 30) | (v & 0x3fffffffu);
+    return (static_cast<uint64_t>(flag_tag(epoch)) << 32) | (static_cast<uint64_t>(st) << 30) | (v & 0x3fffffffu);
 }
 
 // Exclusive prefix sum of n values (n <= 4096) in shared memory by one CTA
@@ -121,7 +126,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_count_kernel(const PlanArgs
     const int E = a.E, K = a.K, R = a.R, C = a.C;
     if (tid == 0) {
         s_tile = static_cast<int>(atomicAdd(&a.hdr->ticket, 1u));
-        s_epoch = *reinterpret_cast<volatile uint32_t*>(&a.hdr->epoch) + 1u;
+        s_epoch = ((*reinterpret_cast<volatile uint32_t*>(&a.hdr->epoch) + 1u) & 0x7fffffffu);
         s_err = 0;
     }
     for (int c = tid; c < C; c += PLAN_THREADS) s_tot[c] = 0;
@@ -193,7 +198,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_count_kernel(const PlanArgs
 #pragma unroll
                         for (int q = 0; q < LOOKBACK_WINDOW; ++q) {
                             if (done || stall) continue;
-                            if (j - q < 0 || static_cast<uint32_t>(w[q] >> 32) != epoch) {
+                            if (j - q < 0 || static_cast<uint32_t>(w[q] >> 32) != flag_tag(epoch)) {
                                 stall = true;
                                 continue;
                             }
@@ -444,7 +449,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_scatter_kernel(const PlanAr
     for (int e = tile; e < E; e += a.T) {
         const int32_t start = __ldg(a.out.zero_fill_ranges + 2 * e);
         const int32_t cnt = __ldg(a.out.zero_fill_ranges + 2 * e + 1);
-        for (int j = tid; j < cnt; j += PLAN_THREADS) a.out.src_of_slot[start + j] = -1;
+        for (int j = tid; j < cnt; j += PLAN_THREADS)
+            if (start >= 0 && static_cast<int64_t>(start) + j < a.p_cap) a.out.src_of_slot[start + j] = -1;
     }
     {
         const int64_t P = __ldg(cu + E);

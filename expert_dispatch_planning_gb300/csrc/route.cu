@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_topk_kernel(const RouteAr
         const float* row = a.logits + (valid ? s : 0) * E;
 
         // ---- load and score
-        float basis[V];  // logit (softmax) or sigmoid (sigmoid scoring)
+        float raw[V];  // logits
         float keyf[V];
         if constexpr (VEC) {
 #pragma unroll
@@ -134,16 +134,16 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_topk_kernel(const RouteAr
                 const int e0 = 4 * (sub + G * j);
                 float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (valid && e0 < E) q = ld_stream_f4(row + e0);
-                basis[4 * j + 0] = q.x;
-                basis[4 * j + 1] = q.y;
-                basis[4 * j + 2] = q.z;
-                basis[4 * j + 3] = q.w;
+                raw[4 * j + 0] = q.x;
+                raw[4 * j + 1] = q.y;
+                raw[4 * j + 2] = q.z;
+                raw[4 * j + 3] = q.w;
             }
         } else {
 #pragma unroll
             for (int v = 0; v < V; ++v) {
                 const int e = sub + G * v;
-                basis[v] = (valid && e < E) ? ld_stream_f32(row + e) : 0.f;
+                raw[v] = (valid && e < E) ? ld_stream_f32(row + e) : 0.f;
             }
         }
         uint32_t key[V];
@@ -151,10 +151,10 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_topk_kernel(const RouteAr
         for (int v = 0; v < V; ++v) {
             const int e = expert_of<G, V, VEC>(sub, v);
             if (sigmoid) {
-                basis[v] = sigmoid_f32(basis[v]);
-                keyf[v] = a.bias != nullptr && e < E ? __fadd_rn(basis[v], __ldg(a.bias + e)) : basis[v];
+                const float sg = sigmoid_f32(raw[v]);
+                keyf[v] = a.bias != nullptr && e < E ? __fadd_rn(sg, __ldg(a.bias + e)) : sg;
             } else {
-                keyf[v] = basis[v];
+                keyf[v] = raw[v];
             }
             key[v] = (valid && e < E) ? order_key(keyf[v]) : 0u;
         }
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_topk_kernel(const RouteAr
                 if (key[v] > bk) {  // values ascend in expert index per lane
                     bk = key[v];
                     bi = static_cast<uint32_t>(expert_of<G, V, VEC>(sub, v));
-                    bv = basis[v];
+                    bv = raw[v];
                 }
             }
             uint32_t wi;
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_topk_kernel(const RouteAr
             win_val[r] = wv;
         }
 
-        // ---- weights
+        // ---- weights (win_val holds the winners' logits)
         float w[KMAX];
         if (!sigmoid) {
             const float m = win_val[0];  // top-1 logit is the row maximum
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_topk_kernel(const RouteAr
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
                     const int e = expert_of<G, V, VEC>(sub, v);
-                    if (valid && e < E) part += static_cast<double>(exp_diff(basis[v], m));
+                    if (valid && e < E) part += static_cast<double>(exp_diff(raw[v], m));
                 }
 #pragma unroll
                 for (int off = 1; off < G; off <<= 1) part += __shfl_xor_sync(FULL_MASK, part, off);
@@ -275,18 +275,28 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_topk_kernel(const RouteAr
                 w[r] = static_cast<float>(static_cast<double>(ek[r]) * scale);
             }
         } else {
+            // scores of the winners; below 2^-100 the fp32 score has lost
+            // relative precision (or underflowed), so fp64 takes over there
+            double sc[KMAX];
             double denom = 0.0;
 #pragma unroll
             for (int r = 0; r < KMAX; ++r) {
                 if (r >= K) break;
-                denom += static_cast<double>(win_val[r]);
+                const float sf = sigmoid_f32(win_val[r]);
+                if (sf < 0x1p-100f) {
+                    const double ex = exp(static_cast<double>(win_val[r]));
+                    sc[r] = ex / (1.0 + ex);
+                } else {
+                    sc[r] = static_cast<double>(sf);
+                }
+                denom += sc[r];
             }
             const double scale = a.renormalize ? static_cast<double>(a.scaling) / denom
                                                : static_cast<double>(a.scaling);
 #pragma unroll
             for (int r = 0; r < KMAX; ++r) {
                 if (r >= K) break;
-                w[r] = static_cast<float>(static_cast<double>(win_val[r]) * scale);
+                w[r] = static_cast<float>(sc[r] * scale);
             }
         }
 

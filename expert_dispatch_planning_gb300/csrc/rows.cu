@@ -247,15 +247,21 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const CombineA
                 }
             }
         } else {
-            for (int c = lane; c < nvec; c += 32) {
+            // shuffles stay in converged code: the chunk loop runs the same
+            // trip count on every lane and predicates the memory accesses
+            for (int c0 = 0; c0 < nvec; c0 += 32) {
+                const int c = c0 + lane;
                 float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                 for (int k = 0; k < K; ++k) {
                     const int32_t raw = __shfl_sync(FULL_MASK, my_raw, k);
                     const float wv = __shfl_sync(FULL_MASK, my_w, k);
-                    const uint4 v = ld_stream_v4(reinterpret_cast<const uint4*>(a.y + static_cast<int64_t>(raw) * H) + c);
-                    fma_row(acc, wv, v);
+                    if (c < nvec) {
+                        const uint4 v =
+                            ld_stream_v4(reinterpret_cast<const uint4*>(a.y + static_cast<int64_t>(raw) * H) + c);
+                        fma_row(acc, wv, v);
+                    }
                 }
-                st_v4(out_row + c, pack_row(acc));
+                if (c < nvec) st_v4(out_row + c, pack_row(acc));
             }
         }
     }
@@ -311,6 +317,7 @@ extern "C" MOE_API int moe_permute(const uint16_t* x, int N, int H, int K, int E
     a.stage_bytes = static_cast<uint32_t>((G * row_bytes + 127) / 128 * 128);
     int stages = env_int("MOE_PERMUTE_STAGES", 4);
     if (stages < 2) stages = 2;
+    if (stages > 16) stages = 16;  // 16 mbarriers fit the 128-byte header
     while (stages > 2 && 128 + 128 + static_cast<size_t>(stages) * a.stage_bytes > kSmemPerSm) --stages;
     a.stages = stages;
     a.slots_bytes = static_cast<uint32_t>((static_cast<int64_t>(stages) * G * K * 4 + 127) / 128 * 128);

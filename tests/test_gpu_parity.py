@@ -60,8 +60,11 @@ def route_both(m, logits, K, bias=None, **kw):
 def check_route(m, logits, K, bias=None, **kw):
     idx, w, o_idx, o_w = route_both(m, logits, K, bias, **kw)
     assert np.array_equal(idx, o_idx), "first mismatch at row %d" % int(np.argwhere((idx != o_idx).any(1))[0][0])
-    rel = np.abs(w.astype(np.float64) - o_w) / np.maximum(np.abs(o_w), 1e-300)
-    assert rel.max() <= 1e-6, rel.max()
+    # 1e-6 relative wherever the exact weight is a normal fp32 number; an
+    # fp32 output cannot carry relative precision below 2^-126
+    err = np.abs(w.astype(np.float64) - o_w)
+    ok = (err <= 1e-6 * np.abs(o_w)) | ((np.abs(o_w) < 2.0 ** -126) & (err <= 2.0 ** -126))
+    assert ok.all(), (err / np.maximum(np.abs(o_w), 1e-300)).max()
     return o_idx, o_w
 
 
@@ -82,7 +85,7 @@ def test_route_configs(m, name):
     (3, 2, 0, 1, 1, 1), (5, 5, 0, 0, 1, 1), (8, 1, 0, 1, 1, 1), (13, 4, 1, 1, 1, 1),
     (16, 3, 0, 0, 1, 1), (32, 8, 1, 0, 1, 1), (64, 6, 0, 1, 1, 1), (100, 7, 1, 1, 4, 2),
     (128, 16, 0, 1, 1, 1), (160, 8, 1, 1, 8, 3), (256, 32, 0, 1, 1, 1), (512, 8, 1, 1, 16, 4),
-    (1024, 8, 0, 0, 1, 1), (1024, 12, 1, 1, 32, 4), (48, 48, 0, 1, 1, 1), (12, 4, 1, 1, 12, 4)])
+    (1024, 8, 0, 0, 1, 1), (1024, 12, 1, 1, 32, 4), (48, 32, 0, 1, 1, 1), (12, 4, 1, 1, 12, 4)])
 def test_route_shapes(m, E, K, scoring, renorm, ng, tg):
     rng = np.random.default_rng(E * 131 + K)
     N = 777
@@ -291,11 +294,14 @@ def test_permute_combine_shapes(m, N, E, K, R, H, a):
 
 
 # ---------------------------------------------------------------- end to end
-@pytest.mark.parametrize("name", ["tiny", "mixtral", "dsv3"])
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "qwen3", "dsv3"])
 def test_end_to_end(m, name):
-    """GPU chain route->plan->permute->combine (identity experts) against the
-    oracle chain; weights differ within 1e-6 so the bf16 output may differ by
-    one rounding step where the fp32 sum sits on a rounding boundary."""
+    """GPU chain route -> plan -> permute -> experts -> combine against the
+    oracle chain, each side computing its own intermediates from the same
+    inputs.  The stand-in experts scale each row by 1 + e/E (bf16, torch on
+    both sides) so the combined sums are not exact bf16 ties.  The weights
+    agree within 1e-6, so an output may differ by one bf16 rounding step
+    where the fp32 sum falls next to a rounding boundary."""
     w = workloads.get(name)
     inp = workloads.make_inputs(w, seed=0)
     lg = torch.from_numpy(inp["logits"]).to(dev())
@@ -304,12 +310,18 @@ def test_end_to_end(m, name):
     idx, wts = m.route_topk(lg, w.K, bias=b, **route_kwargs(w))
     p = m.plan(idx, w.E, w.R, w.alignment)
     perm = m.permute(x, p)
-    out = m.combine(perm, wts, p)
+    cu = p.cu_seqlens.long()
+    row_expert = torch.searchsorted(cu[1:], torch.arange(p.P_cap, device=dev()), right=True).clamp(max=w.E - 1)
+    y = (perm.float() * (1.0 + row_expert.float() / w.E)[:, None]).to(torch.bfloat16)
+    out = m.combine(y, wts, p)
     assert m.get_status(p) == 0
     o_idx, o_w = oracle.route_topk(inp["logits"], w.K, bias=inp["bias"], **route_kwargs(w))
     op = oracle.plan(o_idx, w.E, w.R, w.alignment)
     o_perm = oracle.permute(inp["x_bits"], op["dst"], op["zero_fill_ranges"], w.K, op["P_cap"])
-    o_out = oracle.combine(o_perm, o_w.astype(np.float32), op["dst"])
+    o_rexp = np.minimum(np.searchsorted(op["cu_seqlens"][1:], np.arange(op["P_cap"]), side="right"), w.E - 1)
+    o_y = (torch.from_numpy(o_perm.view(np.int16)).view(torch.bfloat16).float()
+           * torch.from_numpy(1.0 + o_rexp.astype(np.float32) / w.E)[:, None]).to(torch.bfloat16)
+    o_out = oracle.combine(o_y.view(torch.int16).numpy().view(np.uint16), o_w.astype(np.float32), op["dst"])
     g = torch.from_numpy(bits(out).view(np.int16)).view(torch.bfloat16).double().numpy()
     o = torch.from_numpy(o_out.view(np.int16)).view(torch.bfloat16).double().numpy()
     ulp = np.maximum(np.abs(o), 2.0 ** -126) * 2.0 ** -7
