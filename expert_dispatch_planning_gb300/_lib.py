@@ -42,6 +42,7 @@ SIGNATURES = [
     ("moe_plan_workspace_size", _size, [_i32, _i32, _i32, _i32]),
     ("moe_plan_workspace_init", _i32, [_P, _size, _P]),
     ("moe_plan", _i32, [_P, _i32, _i32, _i32, _i32, _i32, _P, _size, ctypes.POINTER(MoePlanOut), _P]),
+    ("moe_plan_no_alloc", _i32, [_P, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(MoePlanOut), _P]),
     ("moe_permute", _i32, [_P, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(MoePlanOut), _P, _P]),
     ("moe_combine", _i32, [_P, _P, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(MoePlanOut), _P, _P]),
     ("moe_get_status", _i32, [ctypes.POINTER(MoePlanOut), ctypes.POINTER(ctypes.c_int32), _P]),

@@ -32,6 +32,8 @@
 //     src_info), is_token_in_rank, and the dedup structures in (token,
 //     first k) order;
 //   - -1 into the padding rows and unused capacity of src_of_slot.
+#include <mutex>
+
 #include "moe_common.cuh"
 
 namespace moe {
@@ -587,4 +589,51 @@ extern "C" MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, in
     rc = moe_host::launch(moe::plan_count_kernel, dim3(g.T), dim3(moe::PLAN_THREADS), smem1, stream, a);
     if (rc != MOE_OK) return rc;
     return moe_host::launch(moe::plan_scatter_kernel, dim3(g.T), dim3(moe::PLAN_THREADS), smem2, stream, a);
+}
+
+// ---------------------------------------------------------------- no-allocation variant
+// Scratch for moe_plan_no_alloc: a fixed device array in this library's
+// module, so the call needs no caller workspace and allocates nothing.
+// Every GPU that loads the library holds these bytes until the process
+// exits.  Host code must not use the symbol itself as a device address; the
+// address comes from cudaGetSymbolAddress once per device.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // 1 MiB
+static __device__ __align__(256) unsigned char g_plan_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  The first call
+// on a device looks the address up and zeroes the array on `stream` (the
+// plan's call counter and look-back flags start from zero).
+int scratch_for_current_device(cudaStream_t stream, void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_plan_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+        if (cudaMemsetAsync(p, 0, kNoAllocScratchBytes, stream) != cudaSuccess) return MOE_ERR_CUDA;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" MOE_API int moe_plan_no_alloc(const int32_t* topk_idx, int N, int E, int K, int R, int alignment,
+                                         const MoePlanOut* out, cudaStream_t stream) {
+    int rc = check_sizes(N, E, K, R);
+    if (rc != MOE_OK) return rc;
+    if (alignment < 1) return MOE_ERR_INVALID_ARG;
+    const size_t need = ws_bytes(plan_geometry(N, E, K, R));
+    if (need > kNoAllocScratchBytes) return MOE_ERR_CAPACITY;
+    void* ws = nullptr;
+    rc = scratch_for_current_device(stream, &ws);
+    if (rc != MOE_OK) return rc;
+    return moe_plan(topk_idx, N, E, K, R, alignment, ws, kNoAllocScratchBytes, out, stream);
 }

@@ -172,6 +172,31 @@ MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, int R, int al
                      void* workspace, size_t workspace_bytes, const MoePlanOut* out,
                      cudaStream_t stream);
 
+/*
+ * moe_plan without a workspace argument, for callers that cannot allocate
+ * device memory: code embedded in a host framework that owns every device
+ * buffer and hands out only inputs and outputs, or latency-critical callers
+ * that must not run cudaMalloc/cudaFree (which can synchronise the whole
+ * device) and have no spare buffer to lend.  The sources have no counterpart:
+ * MoonEP and TensorRT-LLM both take caller- or framework-allocated scratch.
+ *
+ * The plan's scratch lives in a fixed 1 MiB device array inside this library
+ * (every GPU that loads the library holds it until the process exits).  Sizes
+ * whose moe_plan_workspace_size() exceeds 1 MiB return MOE_ERR_CAPACITY; the
+ * five reference workloads (up to N = 65536, E = 256, K = 8, R = 64) need
+ * under 0.6 MiB.  The call allocates nothing and runs the same kernels as
+ * moe_plan, so its outputs are identical.
+ *
+ * The first call on each device looks up the array's device address and
+ * zeroes it with a memset enqueued on `stream`; make that first call before
+ * any stream capture.  All calls on a device share the one array and it keeps
+ * the previous call's state, so calls that may overlap on the GPU (different
+ * streams without ordering between them) race and give wrong plans: order
+ * them on one stream or use moe_plan with separate workspaces.
+ */
+MOE_API int moe_plan_no_alloc(const int32_t* topk_idx, int N, int E, int K, int R, int alignment,
+                              const MoePlanOut* out, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- rows */
 /*
  * Permute (DeepEP dispatch's hidden-row copy, MoonEP dst / zero_fill_ranges):
