@@ -277,14 +277,14 @@ def run_ours(args, w):
 
     for _ in range(max(3, args.warmup)):
         step()
+    launches_per_step = 3 + m.plan_launches(w.N, w.E, w.K, w.R)
     torch.cuda.synchronize()
     status = m.get_status(p)
     if status != 0:
         raise RuntimeError("device status %d during warm-up" % status)
     P = int(p.cu_seqlens[-1].item())
 
-    # ---- timed region: K steps, per-stage events on the launching stream
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    # ---- timed region: K back-to-back steps (launches chained on one stream)
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
@@ -294,11 +294,17 @@ def run_ours(args, w):
         torch.cuda.synchronize()
         start.record(stream)
         for i in range(args.steps):
-            step(evs[i])
+            step()
         stop.record(stream)
         torch.cuda.synchronize()
         barrier()
-    local_ms = start.elapsed_time(stop)
+        local_ms = start.elapsed_time(stop)
+        # ---- the same K steps with an event between stages: per-kernel durations
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            step(evs[i])
+        torch.cuda.synchronize()
     ms = reduce_max(local_ms)
     stage_ms = {k: float(np.mean([e[j].elapsed_time(e[j + 1]) for e in evs]))
                 for j, k in enumerate(["route", "plan", "permute", "combine"])}
@@ -368,12 +374,54 @@ def run_ours(args, w):
         "e2e": {"value": ws * w.N / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h_logits.numel() * 4 + h_x.numel() * 2),
                 "d2h_bytes_per_step": int(h_out.numel() * 2), "ms_per_step": e2e_ms},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)
     if dist.is_initialized():
         dist.destroy_process_group()
+    return 0
+
+
+def run_stage(args, w):
+    """Time one stage alone (inputs resident, K launches back to back)."""
+    import torch
+
+    import expert_dispatch_planning_gb300 as m
+    m.load()
+    dev = torch.device("cuda", 0)
+    inp = workloads.make_inputs(w, seed=0, with_x=args.stage in ("permute", "combine"))
+    logits = torch.from_numpy(inp["logits"]).to(dev)
+    bias = None if inp["bias"] is None else torch.from_numpy(inp["bias"]).to(dev)
+    rk = dict(scoring=w.scoring, renormalize=w.renormalize, bias=bias, n_group=w.n_group,
+              topk_group=w.topk_group, routed_scaling=w.routed_scaling)
+    idx, wts = m.route_topk(logits, w.K, **rk)
+    p = m.plan(idx, w.E, w.R, w.alignment)
+    fns = {"route": lambda: m.route_topk(logits, w.K, topk_idx=idx, topk_w=wts, **rk),
+           "plan": lambda: m.plan(idx, w.E, w.R, w.alignment, out=p)}
+    if args.stage in ("permute", "combine"):
+        x = torch.from_numpy(inp["x_bits"].view(np.int16)).view(torch.bfloat16).to(dev)
+        perm = m.permute(x, p)
+        out = torch.empty_like(x)
+        fns["permute"] = lambda: m.permute(x, p, out=perm)
+        fns["combine"] = lambda: m.combine(perm, wts, p, out=out)
+    fn = fns[args.stage]
+    for _ in range(max(3, args.warmup)):
+        fn()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record()
+    for _ in range(args.steps):
+        fn()
+    ev[1].record()
+    torch.cuda.synchronize()
+    assert m.get_status(p) == 0
+    ms = ev[0].elapsed_time(ev[1]) / args.steps
+    P = int(p.cu_seqlens[-1].item())
+    ab = algorithmic_bytes(w, P)
+    nbytes = ab[args.stage] if args.stage in ab else ab["plan_count"] + ab["plan_scatter"]
+    print(json.dumps({"stage": args.stage, "workload": w.describe(), "us_per_launch": 1e3 * ms,
+                      "algorithmic_bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9}), flush=True)
     return 0
 
 
@@ -385,8 +433,16 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="mixtral", choices=sorted(workloads.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stage", choices=["all", "route", "plan", "permute", "combine"], default="all",
+                    help="time one step of the path alone (a profiling case, not a contract line)")
+    ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count N")
     args = ap.parse_args(argv)
     w = workloads.get(args.config)
+    if args.tokens > 0:
+        import dataclasses
+        w = dataclasses.replace(w, N=args.tokens)
+    if args.stage != "all":
+        return run_stage(args, w)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -40,6 +40,7 @@ SIGNATURES = [
     ("moe_route_topk", _i32, [_P, _P, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _P, _P, _P]),
     ("moe_plan_capacity_rows", _i64, [_i32, _i32, _i32, _i32]),
     ("moe_plan_workspace_size", _size, [_i32, _i32, _i32, _i32]),
+    ("moe_plan_launch_count", _i32, [_i32, _i32, _i32, _i32]),
     ("moe_plan_workspace_init", _i32, [_P, _size, _P]),
     ("moe_plan", _i32, [_P, _i32, _i32, _i32, _i32, _i32, _P, _size, ctypes.POINTER(MoePlanOut), _P]),
     ("moe_plan_no_alloc", _i32, [_P, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(MoePlanOut), _P]),

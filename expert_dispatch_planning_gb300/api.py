@@ -138,6 +138,14 @@ def plan(topk_idx: torch.Tensor, E: int, R: int, alignment: int, out: Plan | Non
     return out
 
 
+def plan_launches(N: int, E: int, K: int, R: int) -> int:
+    """Kernel launches moe_plan makes for these sizes on the current device."""
+    n = int(load().moe_plan_launch_count(N, E, K, R))
+    if n < 0:
+        raise ValueError("unsupported plan sizes")
+    return n
+
+
 def permute(x: torch.Tensor, p: Plan, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Expert-contiguous copy of x bf16[N,H] -> bf16[P_cap,H] (rows >= P untouched)."""
     N, H = x.shape

@@ -32,7 +32,9 @@
 //     src_info), is_token_in_rank, and the dedup structures in (token,
 //     first k) order;
 //   - -1 into the padding rows and unused capacity of src_of_slot.
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "moe_common.cuh"
 
@@ -108,6 +110,234 @@ __device__ void block_exclusive_scan(const int32_t* in, int n, int32_t* out, int
     }
     if (tid == 0) out[n] = s_warp[PLAN_WARPS];
     __syncthreads();
+}
+
+// ---------------------------------------------------------------- shared pieces
+// From the column totals s_tot (E expert counts, R per-rank token counts,
+// groups, duplicates): cu_seqlens into s_cu[0..E] for the calling CTA and,
+// when `write`, every totals-derived output (MoonEP per-rank cu_seqlens and
+// zero_fill_ranges with padded = round_up(count, alignment) for count > 0;
+// DeepEP notify_dispatch rank prefix).  s_pad: E + R + 2 ints of scratch.
+// Contains __syncthreads: every thread of the CTA calls it.
+__device__ void plan_totals(const PlanArgs& a, const int32_t* s_tot, int32_t* s_pad, int32_t* s_cu, int32_t* s_warp,
+                            bool write) {
+    const int tid = threadIdx.x;
+    const int E = a.E, R = a.R, al = a.alignment;
+    for (int e = tid; e < E; e += PLAN_THREADS) {
+        const int32_t c = s_tot[e];
+        s_pad[e] = c > 0 ? static_cast<int32_t>((static_cast<int64_t>(c) + al - 1) / al * al) : 0;
+    }
+    __syncthreads();
+    block_exclusive_scan(s_pad, E, s_cu, s_warp);  // s_cu[0..E] = cu
+    if (!write) return;
+    for (int e = tid; e < E; e += PLAN_THREADS) {
+        a.out.tokens_per_expert[e] = s_tot[e];
+        const int32_t pad = s_pad[e] - s_tot[e];
+        a.out.zero_fill_ranges[2 * e] = pad > 0 ? s_cu[e] + s_tot[e] : 0;
+        a.out.zero_fill_ranges[2 * e + 1] = pad > 0 ? pad : 0;
+    }
+    for (int e = tid; e <= E; e += PLAN_THREADS) a.out.cu_seqlens[e] = s_cu[e];
+    for (int r = tid; r <= R; r += PLAN_THREADS) a.out.rank_slot_offsets[r] = s_cu[r * a.epn];
+    for (int r = tid; r < R; r += PLAN_THREADS) {
+        int32_t pairs = 0;
+        for (int e = r * a.epn; e < (r + 1) * a.epn; ++e) pairs += s_tot[e];
+        a.out.pairs_per_rank[r] = pairs;
+        a.out.tokens_per_rank[r] = s_tot[E + r];
+    }
+    if (tid == 0) {
+        a.out.dup_counts[0] = s_tot[E + R];
+        a.out.dup_counts[1] = s_tot[E + R + 1];
+    }
+    __syncthreads();
+    block_exclusive_scan(s_tot + E, R, s_pad, s_warp);  // s_pad[0..R] = rank prefix
+    for (int r = tid; r <= R; r += PLAN_THREADS) a.out.rank_prefix[r] = s_pad[r];
+}
+
+// Per-pair results of a tile's first pass, kept in registers until the slots
+// are known.
+struct TileItems {
+    int e[PLAN_IPT_MAX];     // expert, -1 for an inactive lane
+    int rank[PLAN_IPT_MAX];  // rank among the same expert's pairs of the warp run
+    int ia[PLAN_IPT_MAX];    // group index (group opener) or duplicate position
+    int ib[PLAN_IPT_MAX];    // first duplicate position of the group (opener)
+    int fl[PLAN_IPT_MAX];    // bit 0 duplicate, bit 1 opens a group, bits 2+ duplicates in it
+};
+
+// First pass over a tile: per-warp running counts of every expert (s_wc,
+// [PLAN_WARPS][E], zeroed), each pair's rank among the same expert's pairs
+// of its warp run (match.any + popc: lanes are in flat-pair order), the
+// duplicate test per (token, rank) (match.any on the pair's token and rank),
+// group / duplicate positions within the warp run (ballots), the tile's
+// is_token_in_rank rows (s_itr, zeroed) and per-warp group / duplicate
+// totals (s_wg, s_wd).  With s_rtok non-null it also counts the tile's
+// tokens per rank.  Reads only topk_idx.
+__device__ __forceinline__ void tile_phase1(const PlanArgs& a, int tile, int32_t* s_wc, uint8_t* s_itr, int32_t* s_wg,
+                                            int32_t* s_wd, int32_t* s_rtok, TileItems& it) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int E = a.E, K = a.K, R = a.R;
+    const int64_t tok0 = static_cast<int64_t>(tile) * a.tile_tokens;
+    const unsigned lt = (1u << lane) - 1u;
+    const int act = a.tpw * K;
+    const int tok_in_iter = lane / K, k = lane - (lane / K) * K;
+    const int tok_lane0 = tok_in_iter * K;
+    const unsigned below_tok = (1u << tok_lane0) - 1u;
+    int run_g = 0, run_d = 0;
+#pragma unroll
+    for (int i = 0; i < PLAN_IPT_MAX; ++i) {
+        it.e[i] = -1;
+        if (i >= a.ipt) continue;
+        const int64_t s = tok0 + static_cast<int64_t>(warp * a.ipt + i) * a.tpw + tok_in_iter;
+        bool active = lane < act && s < a.N;
+        int e = E;
+        if (active) {
+            e = __ldg(a.topk + s * K + k);
+            if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
+                record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(s * K + k));
+                active = false;
+                e = E;
+            }
+        }
+        const unsigned peers = __match_any_sync(FULL_MASK, e);
+        const int base = active ? s_wc[warp * E + e] : 0;
+        const int wr = base + __popc(peers & lt);
+        __syncwarp();
+        if (active && (peers & lt) == 0u) s_wc[warp * E + e] = base + __popc(peers);
+        __syncwarp();
+
+        const int r = active ? e / a.epn : 0;
+        const unsigned key = active ? static_cast<unsigned>(tok_in_iter * 128 + r) : 0xffffffffu;
+        const unsigned pd = __match_any_sync(FULL_MASK, key);
+        const bool prim = active && (pd & lt) == 0u;
+        const bool dup = active && !prim;
+        const bool opens = prim && __popc(pd) >= 2;
+        const unsigned gball = __ballot_sync(FULL_MASK, opens);
+        const unsigned dball = __ballot_sync(FULL_MASK, dup);
+        // duplicates of this token ordered by (primary lane, lane)
+        const int my_p = __ffs(pd) - 1;
+        int before = 0;
+        for (int j = 0; j < K; ++j) {
+            const int lj = (tok_lane0 + j) & 31;
+            const int pj = __shfl_sync(FULL_MASK, my_p, lj);
+            const int dj = __shfl_sync(FULL_MASK, dup ? 1 : 0, lj);
+            if (dj && (pj < my_p || (pj == my_p && lj < lane))) ++before;
+        }
+        const int dup_pos = run_d + __popc(dball & below_tok) + before;
+        if (prim) {
+            s_itr[(s - tok0) * R + r] = 1;
+            if (s_rtok != nullptr) atomicAdd(&s_rtok[r], 1);
+        }
+        if (active) {
+            it.e[i] = e;
+            it.rank[i] = wr;
+            it.fl[i] = (dup ? 1 : 0) | (opens ? 2 : 0) | ((__popc(pd) - 1) << 2);
+            it.ia[i] = opens ? run_g + __popc(gball & lt) : dup_pos;
+            it.ib[i] = dup_pos;
+        }
+        run_g += __popc(gball);
+        run_d += __popc(dball);
+    }
+    if (lane == 0) {
+        s_wg[warp] = run_g;
+        s_wd[warp] = run_d;
+    }
+}
+
+// Second pass over a tile, after the bases are known: s_base[e] = first slot
+// of expert e in this tile, g_base / d_base = groups / duplicates of earlier
+// tiles.  Turns the per-warp counts into per-warp bases, then writes dst,
+// src_of_slot, dup_groups, dup_loffs and the tile's is_token_in_rank rows.
+__device__ __forceinline__ void tile_phase3(const PlanArgs& a, int tile, const int32_t* s_base, int32_t g_base,
+                                            int32_t d_base, int32_t* s_wc, int32_t* s_wg, int32_t* s_wd,
+                                            const uint8_t* s_itr, const TileItems& it) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int E = a.E, K = a.K, R = a.R;
+    const int64_t tok0 = static_cast<int64_t>(tile) * a.tile_tokens;
+    for (int e = tid; e < E; e += PLAN_THREADS) {
+        int32_t run = s_base[e];
+#pragma unroll
+        for (int w = 0; w < PLAN_WARPS; ++w) {
+            const int32_t v = s_wc[w * E + e];
+            s_wc[w * E + e] = run;
+            run += v;
+        }
+    }
+    if (tid == 0) {
+        int32_t g = g_base, d = d_base;
+        for (int w = 0; w < PLAN_WARPS; ++w) {
+            const int32_t vg = s_wg[w], vd = s_wd[w];
+            s_wg[w] = g;
+            s_wd[w] = d;
+            g += vg;
+            d += vd;
+        }
+    }
+    __syncthreads();
+
+    const int tok_in_iter = lane / K, k = lane - (lane / K) * K;
+#pragma unroll
+    for (int i = 0; i < PLAN_IPT_MAX; ++i) {
+        if (it.e[i] < 0) continue;
+        const int e = it.e[i];
+        const int64_t s = tok0 + static_cast<int64_t>(warp * a.ipt + i) * a.tpw + tok_in_iter;
+        const int64_t f = s * K + k;
+        const int32_t slot = s_wc[warp * E + e] + it.rank[i];
+        if (slot < 0 || static_cast<int64_t>(slot) >= a.p_cap) {
+            record_error(a.out.status, MOE_ERR_DEVICE_INDEX, slot);
+            continue;
+        }
+        const bool dup = it.fl[i] & 1;
+        a.out.dst[f] = dup ? -slot - 1 : slot;
+        a.out.src_of_slot[slot] = static_cast<int32_t>(f);
+        if (it.fl[i] & 2) {
+            const int64_t g = static_cast<int64_t>(s_wg[warp]) + it.ia[i];
+            if (g >= static_cast<int64_t>(a.N) * (K / 2)) {
+                record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(g));
+                continue;
+            }
+            int32_t* row = a.out.dup_groups + 3 * g;
+            row[0] = slot;
+            row[1] = s_wd[warp] + it.ib[i];
+            row[2] = it.fl[i] >> 2;
+        } else if (dup) {
+            const int64_t pos = static_cast<int64_t>(s_wd[warp]) + it.ia[i];
+            if (pos >= static_cast<int64_t>(a.N) * (K - 1)) {
+                record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(pos));
+                continue;
+            }
+            a.out.dup_loffs[pos] = slot;
+        }
+    }
+
+    // is_token_in_rank rows of this tile (16-byte stores when aligned)
+    const int64_t ntok = min(static_cast<int64_t>(a.tile_tokens), static_cast<int64_t>(a.N) - tok0);
+    const int64_t nbytes = ntok * R;
+    uint8_t* g = a.out.is_token_in_rank + tok0 * R;
+    if ((reinterpret_cast<uintptr_t>(g) & 15u) == 0) {
+        const int64_t nvec = nbytes / 16;
+        for (int64_t v = tid; v < nvec; v += PLAN_THREADS)
+            reinterpret_cast<uint4*>(g)[v] = reinterpret_cast<const uint4*>(s_itr)[v];
+        for (int64_t b = nvec * 16 + tid; b < nbytes; b += PLAN_THREADS) g[b] = s_itr[b];
+    } else {
+        for (int64_t b = tid; b < nbytes; b += PLAN_THREADS) g[b] = s_itr[b];
+    }
+}
+
+// -1 into src_of_slot for the padding rows of experts tile, tile + T, ...
+// (cu, cnt: cu_seqlens and per-expert counts) and for this tile's share of
+// the unused rows [P, P_cap).
+__device__ __forceinline__ void fill_unused(const PlanArgs& a, int tile, int T, const int32_t* cu, const int32_t* cnt) {
+    const int tid = threadIdx.x;
+    for (int e = tile; e < a.E; e += T) {
+        const int32_t start = cu[e] + cnt[e];
+        const int32_t n = cu[e + 1] - start;
+        for (int j = tid; j < n; j += PLAN_THREADS)
+            if (start >= 0 && static_cast<int64_t>(start) + j < a.p_cap) a.out.src_of_slot[start + j] = -1;
+    }
+    const int64_t P = cu[a.E];
+    const int64_t rest = a.p_cap - P;
+    const int64_t per = (rest + T - 1) / T;
+    const int64_t b = P + per * tile, e = min(a.p_cap, b + per);
+    for (int64_t j = b + tid; j < e; j += PLAN_THREADS) a.out.src_of_slot[j] = -1;
 }
 
 // ---------------------------------------------------------------- launch 1
@@ -239,36 +469,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_count_kernel(const PlanArgs
         __syncthreads();
 
         // ---- last tile: totals -> aligned offsets and rank arrays
-        if (tile == a.T - 1 && tile != a.skip_tile && s_err == 0) {
-            const int al = a.alignment;
-            for (int e = tid; e < E; e += PLAN_THREADS) {
-                const int32_t c = s_tot[e];
-                s_tmp[e] = c > 0 ? static_cast<int32_t>((static_cast<int64_t>(c) + al - 1) / al * al) : 0;
-                a.out.tokens_per_expert[e] = c;
-            }
-            __syncthreads();
-            block_exclusive_scan(s_tmp, E, s_scan, s_warp);  // s_scan[0..E] = cu
-            for (int e = tid; e <= E; e += PLAN_THREADS) a.out.cu_seqlens[e] = s_scan[e];
-            for (int e = tid; e < E; e += PLAN_THREADS) {
-                const int32_t pad = s_tmp[e] - s_tot[e];
-                a.out.zero_fill_ranges[2 * e] = pad > 0 ? s_scan[e] + s_tot[e] : 0;
-                a.out.zero_fill_ranges[2 * e + 1] = pad > 0 ? pad : 0;
-            }
-            for (int r = tid; r <= R; r += PLAN_THREADS) a.out.rank_slot_offsets[r] = s_scan[r * a.epn];
-            for (int r = tid; r < R; r += PLAN_THREADS) {
-                int32_t pairs = 0;
-                for (int e = r * a.epn; e < (r + 1) * a.epn; ++e) pairs += s_tot[e];
-                a.out.pairs_per_rank[r] = pairs;
-                a.out.tokens_per_rank[r] = s_tot[E + r];
-            }
-            if (tid == 0) {
-                a.out.dup_counts[0] = s_tot[E + R];
-                a.out.dup_counts[1] = s_tot[E + R + 1];
-            }
-            __syncthreads();
-            block_exclusive_scan(s_tot + E, R, s_tmp, s_warp);  // s_tmp[0..R] = rank prefix
-            for (int r = tid; r <= R; r += PLAN_THREADS) a.out.rank_prefix[r] = s_tmp[r];
-        }
+        if (tile == a.T - 1 && tile != a.skip_tile && s_err == 0) plan_totals(a, s_tot, s_tmp, s_scan, s_warp, true);
     }
 
     // ---- completion: the last CTA to finish closes the epoch
@@ -288,84 +489,23 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_count_kernel(const PlanArgs
 // ---------------------------------------------------------------- launch 2
 __global__ void __launch_bounds__(PLAN_THREADS) plan_scatter_kernel(const PlanArgs a) {
     extern __shared__ __align__(16) int32_t s_dyn[];
-    int32_t* s_wc = s_dyn;                                              // [PLAN_WARPS][E]
-    uint8_t* s_itr = reinterpret_cast<uint8_t*>(s_dyn + PLAN_WARPS * a.E);  // [tile_tokens][R]
+    int32_t* s_wc = s_dyn;                                             // [PLAN_WARPS][E]
+    int32_t* s_base = s_wc + PLAN_WARPS * a.E;                         // [E]
+    uint8_t* s_itr = reinterpret_cast<uint8_t*>(s_base + a.E);         // [tile_tokens][R]
     __shared__ int32_t s_wg[PLAN_WARPS], s_wd[PLAN_WARPS];
     __shared__ int32_t s_bad;
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int E = a.E, K = a.K, R = a.R;
+    const int tid = threadIdx.x;
+    const int E = a.E, R = a.R;
     const int tile = blockIdx.x;
-    const int64_t tok0 = static_cast<int64_t>(tile) * a.tile_tokens;
     const int itr_bytes = a.tile_tokens * R;
-
     for (int i = tid; i < PLAN_WARPS * E; i += PLAN_THREADS) s_wc[i] = 0;
     for (int i = tid; i < (itr_bytes + 3) / 4; i += PLAN_THREADS) reinterpret_cast<int32_t*>(s_itr)[i] = 0;
     __syncthreads();
 
-    // ---- phase 1: ranks within the warp run, duplicate bookkeeping.  Reads
-    // only topk_idx, which was complete before launch 1 passed its wait.
-    const unsigned lt = (1u << lane) - 1u;
-    const int act = a.tpw * K;
-    const int tok_in_iter = lane / K, k = lane - (lane / K) * K;
-    const int tok_lane0 = tok_in_iter * K;
-    const unsigned below_tok = (1u << tok_lane0) - 1u;
-    int it_e[PLAN_IPT_MAX], it_rank[PLAN_IPT_MAX], it_a[PLAN_IPT_MAX], it_b[PLAN_IPT_MAX], it_f[PLAN_IPT_MAX];
-    int run_g = 0, run_d = 0;
-#pragma unroll
-    for (int i = 0; i < PLAN_IPT_MAX; ++i) {
-        it_e[i] = -1;
-        if (i >= a.ipt) continue;
-        const int64_t s = tok0 + static_cast<int64_t>(warp * a.ipt + i) * a.tpw + tok_in_iter;
-        bool active = lane < act && s < a.N;
-        int e = E;
-        if (active) {
-            e = __ldg(a.topk + s * K + k);
-            if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
-                active = false;
-                e = E;
-            }
-        }
-        const unsigned peers = __match_any_sync(FULL_MASK, e);
-        const int base = active ? s_wc[warp * E + e] : 0;
-        const int wr = base + __popc(peers & lt);
-        __syncwarp();
-        if (active && (peers & lt) == 0u) s_wc[warp * E + e] = base + __popc(peers);
-        __syncwarp();
-
-        const int r = active ? e / a.epn : 0;
-        const unsigned key = active ? static_cast<unsigned>(tok_in_iter * 128 + r) : 0xffffffffu;
-        const unsigned pd = __match_any_sync(FULL_MASK, key);
-        const bool prim = active && (pd & lt) == 0u;
-        const bool dup = active && !prim;
-        const bool opens = prim && __popc(pd) >= 2;
-        const unsigned gball = __ballot_sync(FULL_MASK, opens);
-        const unsigned dball = __ballot_sync(FULL_MASK, dup);
-        // duplicates of this token ordered by (primary lane, lane)
-        const int my_p = __ffs(pd) - 1;
-        int before = 0;
-        for (int j = 0; j < K; ++j) {
-            const int lj = (tok_lane0 + j) & 31;
-            const int pj = __shfl_sync(FULL_MASK, my_p, lj);
-            const int dj = __shfl_sync(FULL_MASK, dup ? 1 : 0, lj);
-            if (dj && (pj < my_p || (pj == my_p && lj < lane))) ++before;
-        }
-        const int dup_pos = run_d + __popc(dball & below_tok) + before;
-        if (prim) s_itr[(s - tok0) * R + r] = 1;
-        if (active) {
-            it_e[i] = e;
-            it_rank[i] = wr;
-            it_f[i] = (dup ? 1 : 0) | (opens ? 2 : 0) | ((__popc(pd) - 1) << 2);
-            it_a[i] = opens ? run_g + __popc(gball & lt) : dup_pos;
-            it_b[i] = dup_pos;
-        }
-        run_g += __popc(gball);
-        run_d += __popc(dball);
-    }
-    if (lane == 0) {
-        s_wg[warp] = run_g;
-        s_wd[warp] = run_d;
-    }
+    // Reads only topk_idx, which was complete before launch 1 passed its wait.
+    TileItems it;
+    tile_phase1(a, tile, s_wc, s_itr, s_wg, s_wd, nullptr, it);
 
     // ---- everything below needs launch 1's outputs
     pdl_wait();
@@ -373,94 +513,114 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_scatter_kernel(const PlanAr
     if (tid == 0) s_bad = ld_volatile_s32(a.out.status) != 0 ? 1 : 0;
     __syncthreads();
     if (s_bad) return;
-
-    const int32_t* cu = a.out.cu_seqlens;
     const int32_t* tp = a.tile_prefix + static_cast<size_t>(tile) * a.C;
-    for (int e = tid; e < E; e += PLAN_THREADS) {
-        int32_t run = __ldg(cu + e) + __ldg(tp + e);
-#pragma unroll
-        for (int w = 0; w < PLAN_WARPS; ++w) {
-            const int32_t v = s_wc[w * E + e];
-            s_wc[w * E + e] = run;
-            run += v;
-        }
-    }
-    if (tid == 0) {
-        int32_t g = __ldg(tp + E + R), d = __ldg(tp + E + R + 1);
-        for (int w = 0; w < PLAN_WARPS; ++w) {
-            const int32_t vg = s_wg[w], vd = s_wd[w];
-            s_wg[w] = g;
-            s_wd[w] = d;
-            g += vg;
-            d += vd;
-        }
-    }
+    for (int e = tid; e < E; e += PLAN_THREADS) s_base[e] = __ldg(a.out.cu_seqlens + e) + __ldg(tp + e);
+    const int32_t g_base = __ldg(tp + E + R), d_base = __ldg(tp + E + R + 1);
+    __syncthreads();
+    tile_phase3(a, tile, s_base, g_base, d_base, s_wc, s_wg, s_wd, s_itr, it);
+    fill_unused(a, tile, a.T, a.out.cu_seqlens, a.out.tokens_per_expert);
+}
+
+// ---------------------------------------------------------------- cluster path
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+// Address of `p` (this CTA's shared memory) in the shared memory of CTA
+// `rank` of the cluster, then a load from it.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ int32_t ld_dsmem_s32(uint32_t addr) {
+    int32_t v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// The whole plan in one launch for up to 16 tiles: one thread-block
+// cluster, one CTA per tile.  Each CTA runs the tile's first pass, publishes
+// its column counts in its own shared memory, and after a cluster barrier
+// reads the other CTAs' counts through distributed shared memory: the sum
+// over lower ranks is its exclusive prefix, the sum over all its totals.
+// Every CTA scans the totals into cu_seqlens itself; rank 0 writes the
+// totals-derived outputs.  No workspace, no look-back, no spin.
+__global__ void __launch_bounds__(PLAN_THREADS) plan_cluster_kernel(const PlanArgs a) {
+    extern __shared__ __align__(16) int32_t s_dyn[];
+    const int E = a.E, R = a.R, C = a.C;
+    int32_t* s_wc = s_dyn;                        // [PLAN_WARPS][E]
+    int32_t* s_cnt = s_wc + PLAN_WARPS * E;       // [C]  this tile's column counts
+    int32_t* s_tot = s_cnt + C;                   // [C]  cluster totals
+    int32_t* s_base = s_tot + C;                  // [E]
+    int32_t* s_pad = s_base + E;                  // [E + R + 2]
+    int32_t* s_cu = s_pad + E + R + 2;            // [E + R + 2]
+    uint8_t* s_itr = reinterpret_cast<uint8_t*>(s_cu + E + R + 2);  // [tile_tokens][R]
+    __shared__ int32_t s_wg[PLAN_WARPS], s_wd[PLAN_WARPS], s_warp[PLAN_WARPS + 1];
+    __shared__ int32_t s_gd[2];
+
+    pdl_wait();
+    pdl_trigger();
+    const int tid = threadIdx.x;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t ncta = cluster_nctarank();
+    const int tile = static_cast<int>(rank);
+    const int itr_bytes = a.tile_tokens * R;
+    for (int i = tid; i < PLAN_WARPS * E; i += PLAN_THREADS) s_wc[i] = 0;
+    for (int i = tid; i < (itr_bytes + 3) / 4; i += PLAN_THREADS) reinterpret_cast<int32_t*>(s_itr)[i] = 0;
+    for (int c = E + tid; c < C; c += PLAN_THREADS) s_cnt[c] = 0;
     __syncthreads();
 
-    // ---- phase 3: slots, dst, provenance, dedup structures
+    TileItems it;
+    tile_phase1(a, tile, s_wc, s_itr, s_wg, s_wd, s_cnt + E, it);
+    __syncthreads();
+    for (int e = tid; e < E; e += PLAN_THREADS) {
+        int32_t c = 0;
 #pragma unroll
-    for (int i = 0; i < PLAN_IPT_MAX; ++i) {
-        if (it_e[i] < 0) continue;
-        const int e = it_e[i];
-        const int64_t s = tok0 + static_cast<int64_t>(warp * a.ipt + i) * a.tpw + tok_in_iter;
-        const int64_t f = s * K + k;
-        const int32_t slot = s_wc[warp * E + e] + it_rank[i];
-        if (slot < 0 || static_cast<int64_t>(slot) >= a.p_cap) {
-            record_error(a.out.status, MOE_ERR_DEVICE_INDEX, slot);
-            continue;
-        }
-        const bool dup = it_f[i] & 1;
-        a.out.dst[f] = dup ? -slot - 1 : slot;
-        a.out.src_of_slot[slot] = static_cast<int32_t>(f);
-        if (it_f[i] & 2) {
-            const int64_t g = static_cast<int64_t>(s_wg[warp]) + it_a[i];
-            if (g >= static_cast<int64_t>(a.N) * (K / 2)) {
-                record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(g));
-                continue;
-            }
-            int32_t* row = a.out.dup_groups + 3 * g;
-            row[0] = slot;
-            row[1] = s_wd[warp] + it_b[i];
-            row[2] = it_f[i] >> 2;
-        } else if (dup) {
-            const int64_t pos = static_cast<int64_t>(s_wd[warp]) + it_a[i];
-            if (pos >= static_cast<int64_t>(a.N) * (K - 1)) {
-                record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(pos));
-                continue;
-            }
-            a.out.dup_loffs[pos] = slot;
-        }
+        for (int w = 0; w < PLAN_WARPS; ++w) c += s_wc[w * E + e];
+        s_cnt[e] = c;
     }
+    if (tid == 0) {
+        int32_t g = 0, d = 0;
+        for (int w = 0; w < PLAN_WARPS; ++w) {
+            g += s_wg[w];
+            d += s_wd[w];
+        }
+        s_cnt[E + R] = g;
+        s_cnt[E + R + 1] = d;
+    }
+    cluster_arrive();  // counts of every tile visible cluster-wide
+    cluster_wait();
 
-    // ---- is_token_in_rank rows of this tile (16-byte stores when aligned)
-    {
-        const int64_t ntok = min(static_cast<int64_t>(a.tile_tokens), static_cast<int64_t>(a.N) - tok0);
-        const int64_t nbytes = ntok * R;
-        uint8_t* g = a.out.is_token_in_rank + tok0 * R;
-        if ((reinterpret_cast<uintptr_t>(g) & 15u) == 0) {
-            const int64_t nvec = nbytes / 16;
-            for (int64_t v = tid; v < nvec; v += PLAN_THREADS)
-                reinterpret_cast<uint4*>(g)[v] = reinterpret_cast<const uint4*>(s_itr)[v];
-            for (int64_t b = nvec * 16 + tid; b < nbytes; b += PLAN_THREADS) g[b] = s_itr[b];
-        } else {
-            for (int64_t b = tid; b < nbytes; b += PLAN_THREADS) g[b] = s_itr[b];
+    for (int c = tid; c < C; c += PLAN_THREADS) {
+        int32_t excl = 0, tot = 0;
+        for (uint32_t q = 0; q < ncta; ++q) {
+            const int32_t v = ld_dsmem_s32(dsmem_addr(s_cnt + c, q));
+            if (q < rank) excl += v;
+            tot += v;
         }
+        s_tot[c] = tot;
+        if (c < E) s_base[c] = excl;
+        if (c == E + R) s_gd[0] = excl;
+        if (c == E + R + 1) s_gd[1] = excl;
     }
+    cluster_arrive();  // done reading the other CTAs' shared memory
+    __syncthreads();
 
-    // ---- -1 into padding rows (experts tile, tile+T, ...) and unused rows
-    for (int e = tile; e < E; e += a.T) {
-        const int32_t start = __ldg(a.out.zero_fill_ranges + 2 * e);
-        const int32_t cnt = __ldg(a.out.zero_fill_ranges + 2 * e + 1);
-        for (int j = tid; j < cnt; j += PLAN_THREADS)
-            if (start >= 0 && static_cast<int64_t>(start) + j < a.p_cap) a.out.src_of_slot[start + j] = -1;
-    }
-    {
-        const int64_t P = __ldg(cu + E);
-        const int64_t rest = a.p_cap - P;
-        const int64_t per = (rest + a.T - 1) / a.T;
-        const int64_t b = P + per * tile, e = min(a.p_cap, b + per);
-        for (int64_t j = b + tid; j < e; j += PLAN_THREADS) a.out.src_of_slot[j] = -1;
-    }
+    plan_totals(a, s_tot, s_pad, s_cu, s_warp, rank == 0);
+    for (int e = tid; e < E; e += PLAN_THREADS) s_base[e] += s_cu[e];
+    __syncthreads();
+    tile_phase3(a, tile, s_base, s_gd[0], s_gd[1], s_wc, s_wg, s_wd, s_itr, it);
+    fill_unused(a, tile, static_cast<int>(ncta), s_cu, s_tot);
+    cluster_wait();  // keep this CTA's shared memory alive until all reads are done
 }
 
 }  // namespace moe
@@ -518,6 +678,79 @@ int check_sizes(int N, int E, int K, int R) {
 
 }  // namespace
 
+namespace {
+
+constexpr int kMaxClusterTiles = 16;
+
+// Tiles for the one-launch cluster path: as few iterations per warp as keep
+// the tile count within 16.  False when the plan needs more tiles, when the
+// tile's is_token_in_rank rows exceed 64 KB, or when MOE_PLAN_CLUSTER=0.
+bool cluster_geometry(int N, int E, int K, int R, Geom* g) {
+    if (env_int("MOE_PLAN_CLUSTER", 1) == 0) return false;
+    g->tpw = 32 / K;
+    const int64_t per_tile_iter = static_cast<int64_t>(moe::PLAN_WARPS) * g->tpw;  // tokens
+    const int64_t tiles1 = (static_cast<int64_t>(N) + per_tile_iter - 1) / per_tile_iter;
+    const int64_t ipt = (tiles1 + kMaxClusterTiles - 1) / kMaxClusterTiles;
+    if (ipt > moe::PLAN_IPT_MAX) return false;
+    g->ipt = static_cast<int>(ipt < 1 ? 1 : ipt);
+    g->tile_tokens = moe::PLAN_WARPS * g->ipt * g->tpw;
+    if (static_cast<int64_t>(g->tile_tokens) * R > 65536) return false;
+    g->T = static_cast<int>((static_cast<int64_t>(N) + g->tile_tokens - 1) / g->tile_tokens);
+    g->C = E + R + 2;
+    return g->T >= 1 && g->T <= kMaxClusterTiles;
+}
+
+size_t cluster_smem(const Geom& g, int E, int R) {
+    const size_t ints = static_cast<size_t>(moe::PLAN_WARPS) * E + 2 * static_cast<size_t>(g.C) + E +
+                        2 * static_cast<size_t>(E + R + 2);
+    return sizeof(int32_t) * ints + (static_cast<size_t>(g.tile_tokens) * R + 15) / 16 * 16;
+}
+
+cudaLaunchConfig_t cluster_config(int T, size_t smem, cudaStream_t stream, cudaLaunchAttribute* attr, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(T);
+    cfg.blockDim = dim3(moe::PLAN_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = T;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cfg;
+}
+
+// Whether a cluster of T CTAs with this much shared memory fits the GPU
+// (cached per device, size and shared memory).
+bool cluster_launchable(int T, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, size_t>, bool> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const auto key = std::make_tuple(dev, T, smem);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = cluster_config(T, smem, nullptr, attr, false);
+    int n = 0;
+    const bool ok = cudaOccupancyMaxActiveClusters(&n, moe::plan_cluster_kernel, &cfg) == cudaSuccess && n >= 1;
+    if (!ok) cudaGetLastError();  // clear a sticky-free query error
+    cache[key] = ok;
+    return ok;
+}
+
+int launch_cluster(const PlanArgs& a, size_t smem, cudaStream_t stream) {
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = cluster_config(a.T, smem, stream, attr, moe_host::pdl_enabled());
+    return cudaLaunchKernelEx(&cfg, moe::plan_cluster_kernel, a) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
 extern "C" MOE_API int64_t moe_plan_capacity_rows(int N, int E, int K, int alignment) {
     if (N < 1 || E < 1 || K < 1 || alignment < 1) return -1;
     return static_cast<int64_t>(N) * K + static_cast<int64_t>(E) * (alignment - 1);
@@ -526,6 +759,22 @@ extern "C" MOE_API int64_t moe_plan_capacity_rows(int N, int E, int K, int align
 extern "C" MOE_API size_t moe_plan_workspace_size(int N, int E, int K, int R) {
     if (check_sizes(N, E, K, R) != MOE_OK) return 0;
     return ws_bytes(plan_geometry(N, E, K, R));
+}
+
+extern "C" MOE_API int moe_plan_launch_count(int N, int E, int K, int R) {
+    if (check_sizes(N, E, K, R) != MOE_OK) return -1;
+    Geom cg;
+    if (cluster_geometry(N, E, K, R, &cg)) {
+        const int big = 200 * 1024;
+        if (cudaFuncSetAttribute(moe::plan_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, big) ==
+                cudaSuccess &&
+            cudaFuncSetAttribute(moe::plan_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                cudaSuccess &&
+            cluster_launchable(cg.T, cluster_smem(cg, E, R)))
+            return 1;
+        cudaGetLastError();
+    }
+    return 2;
 }
 
 extern "C" MOE_API int moe_plan_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream) {
@@ -574,18 +823,34 @@ extern "C" MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, in
     a.skip_tile = moe_host::skip_tile();
     a.timeout_ns = moe_host::timeout_ns();
 
-    const size_t smem1 = sizeof(int32_t) * (static_cast<size_t>(g.C) + 2 * (E + R + 2) + 2);
-    const size_t smem2 = sizeof(int32_t) * static_cast<size_t>(moe::PLAN_WARPS) * E +
-                         (static_cast<size_t>(g.tile_tokens) * R + 15) / 16 * 16;
-    static bool attr_done = false;
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(moe::plan_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(moe::plan_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) !=
-                cudaSuccess)
-            return MOE_ERR_CUDA;
-        attr_done = true;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        const int big = 200 * 1024;
+        cudaError_t e1 = cudaFuncSetAttribute(moe::plan_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+        cudaError_t e2 = cudaFuncSetAttribute(moe::plan_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+        cudaError_t e3 = cudaFuncSetAttribute(moe::plan_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+        cudaError_t e4 = cudaFuncSetAttribute(moe::plan_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        attr_err = e1 != cudaSuccess ? e1 : e2 != cudaSuccess ? e2 : e3 != cudaSuccess ? e3 : e4;
+    });
+    if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
+
+    // ---- one launch: a thread-block cluster of up to 16 tiles
+    Geom cg;
+    if (cluster_geometry(N, E, K, R, &cg)) {
+        PlanArgs c = a;
+        c.tpw = cg.tpw;
+        c.ipt = cg.ipt;
+        c.tile_tokens = cg.tile_tokens;
+        c.T = cg.T;
+        const size_t smem = cluster_smem(cg, E, R);
+        if (cluster_launchable(cg.T, smem)) return launch_cluster(c, smem, stream);
     }
+
+    // ---- two launches: decoupled look-back over tiles, then the scatter
+    const size_t smem1 = sizeof(int32_t) * (static_cast<size_t>(g.C) + 2 * (E + R + 2) + 2);
+    const size_t smem2 = sizeof(int32_t) * static_cast<size_t>(moe::PLAN_WARPS + 1) * E +
+                         (static_cast<size_t>(g.tile_tokens) * R + 15) / 16 * 16;
     rc = moe_host::launch(moe::plan_count_kernel, dim3(g.T), dim3(moe::PLAN_THREADS), smem1, stream, a);
     if (rc != MOE_OK) return rc;
     return moe_host::launch(moe::plan_scatter_kernel, dim3(g.T), dim3(moe::PLAN_THREADS), smem2, stream, a);

@@ -143,6 +143,16 @@ MOE_API int64_t moe_plan_capacity_rows(int N, int E, int K, int alignment);
 MOE_API size_t moe_plan_workspace_size(int N, int E, int K, int R);
 
 /*
+ * Kernel launches moe_plan makes for these sizes on the current device: 1
+ * when the plan fits one thread-block cluster of up to 16 tiles (one tile =
+ * 16 warps x up to 8 steps x floor(32/K) tokens) and the GPU can co-schedule
+ * it, else 2 (decoupled look-back, then the scatter).  -1 on bad sizes.
+ * Setting the environment variable MOE_PLAN_CLUSTER=0 forces the 2-launch
+ * path; both produce identical plans.
+ */
+MOE_API int moe_plan_launch_count(int N, int E, int K, int R);
+
+/*
  * Prepare a workspace for its first use (enqueues a memset on `stream`).
  * A workspace carries a call counter between calls, so it must be
  * initialised once after allocation; afterwards any number of moe_plan

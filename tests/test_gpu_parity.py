@@ -118,8 +118,17 @@ def plan_both(m, topk, E, R, a, out=None):
     return p, got, want
 
 
+@pytest.fixture(params=["auto", "lookback"])
+def plan_path(request, monkeypatch):
+    """auto: one-launch cluster plan where the plan fits 16 tiles, else the
+    two-launch look-back plan; lookback: the look-back plan everywhere."""
+    if request.param == "lookback":
+        monkeypatch.setenv("MOE_PLAN_CLUSTER", "0")
+    return request.param
+
+
 @pytest.mark.parametrize("name", ["tiny", "mixtral", "qwen3", "dsv3", "large"])
-def test_plan_configs(m, name):
+def test_plan_configs(m, name, plan_path):
     w = workloads.get(name)
     inp = workloads.make_inputs(w, seed=0, with_x=False)
     o_idx, _ = oracle.route_topk(inp["logits"], w.K, bias=inp["bias"], **route_kwargs(w))
@@ -135,7 +144,7 @@ def test_plan_configs(m, name):
     (5000, 32, 6, 32, 7, "rand"), (2500, 128, 16, 8, 64, "rand"), (700, 64, 32, 2, 2, "rand"),
     (9000, 8, 2, 4, 16, "hot"), (3000, 1024, 8, 128, 128, "rand"), (2049, 24, 5, 3, 9, "dups"),
     (600, 16, 4, 4, 5, "one"), (12345, 256, 8, 64, 128, "rand"), (20000, 96, 1, 96, 32, "rand")])
-def test_plan_shapes(m, N, E, K, R, a, mode):
+def test_plan_shapes(m, N, E, K, R, a, mode, plan_path):
     rng = np.random.default_rng(N + E + K)
     if mode == "one":      # every pair on expert 3: empty experts, one full
         topk = np.full((N, K), 3, np.int32)
@@ -149,7 +158,7 @@ def test_plan_shapes(m, N, E, K, R, a, mode):
     check_plan_invariants(got, topk, E, R, a)
 
 
-def test_plan_workspace_reuse_across_calls_and_sizes(m):
+def test_plan_workspace_reuse_across_calls_and_sizes(m, plan_path):
     rng = np.random.default_rng(9)
     E, R, a = 64, 8, 16
     big = m.Plan.allocate(6000, E, 8, R, a)
@@ -170,7 +179,8 @@ def test_plan_bad_expert_id_reports_device_index(m):
     assert m.get_status(p) == 6
 
 
-def test_plan_uninitialised_workspace_reports_error(m):
+def test_plan_uninitialised_workspace_reports_error(m, monkeypatch):
+    monkeypatch.setenv("MOE_PLAN_CLUSTER", "0")   # the look-back path is the one with a workspace
     topk = workloads.random_topk(np.random.default_rng(3), 4000, 16, 4)
     t = torch.from_numpy(topk).to(dev())
     p = m.Plan.allocate(4000, 16, 4, 4, 8)
