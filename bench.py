@@ -284,30 +284,47 @@ def run_ours(args, w):
         raise RuntimeError("device status %d during warm-up" % status)
     P = int(p.cu_seqlens[-1].item())
 
-    # ---- timed region: K back-to-back steps (launches chained on one stream)
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
+    # ---- one step (and each stage alone) captured as CUDA graphs: the
+    # timed region replays them, so host-side launch cost is not measured
+    graph_stream = torch.cuda.Stream()
+    graph_stream.wait_stream(stream)
+    graphs = {}
+    with torch.cuda.stream(graph_stream):
+        for name, fn in (("step", step), ("route", lambda: m.route_topk(logits, w.K, topk_idx=idx, topk_w=wts, **rk)),
+                         ("plan", lambda: m.plan(idx, w.E, w.R, w.alignment, out=p)),
+                         ("permute", lambda: m.permute(x, p, out=perm)),
+                         ("combine", lambda: m.combine(perm, wts, p, out=out))):
+            fn()  # warm on the capture stream
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=graph_stream):
+                fn()
+            graphs[name] = g
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def timed(g, reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    for _ in range(max(3, args.warmup)):
+        graphs["step"].replay()
+    torch.cuda.synchronize()
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[torch.cuda.current_device()]))
     with clocks:
         barrier()
         torch.cuda.synchronize()
-        start.record(stream)
-        for i in range(args.steps):
-            step()
-        stop.record(stream)
-        torch.cuda.synchronize()
+        local_ms = timed(graphs["step"], args.steps)  # the timed region: K steps
         barrier()
-        local_ms = start.elapsed_time(stop)
-        # ---- the same K steps with an event between stages: per-kernel durations
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-        torch.cuda.synchronize()
-        for i in range(args.steps):
-            step(evs[i])
-        torch.cuda.synchronize()
+        # each kernel alone, same inputs, for its achieved bandwidth
+        stage_ms = {k: timed(graphs[k], args.steps) / args.steps for k in ("route", "plan", "permute", "combine")}
     ms = reduce_max(local_ms)
-    stage_ms = {k: float(np.mean([e[j].elapsed_time(e[j + 1]) for e in evs]))
-                for j, k in enumerate(["route", "plan", "permute", "combine"])}
     assert m.get_status(p) == 0
 
     # ---- end to end through host buffers (pinned), copies inside the region
@@ -363,7 +380,8 @@ def run_ours(args, w):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_of(w, extra={"P": P, "l2": "inputs larger than L2 (%.0f MB touched per step)"
                                       % (sum(ab[k] for k in ("permute", "combine")) / 1e6),
-                                      "experts": "identity (combine reads the permuted rows)"}),
+                                      "experts": "identity (combine reads the permuted rows)",
+                                      "launch": "CUDA graph of one step, replayed K times"}),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "traffic": committed_traffic(dom, w.name),
@@ -406,13 +424,21 @@ def run_stage(args, w):
         fns["permute"] = lambda: m.permute(x, p, out=perm)
         fns["combine"] = lambda: m.combine(perm, wts, p, out=out)
     fn = fns[args.stage]
-    for _ in range(max(3, args.warmup)):
+    gs = torch.cuda.Stream()
+    gs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(gs):
         fn()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gs):
+            fn()
+    torch.cuda.synchronize()
+    for _ in range(max(3, args.warmup)):
+        g.replay()
     torch.cuda.synchronize()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     ev[0].record()
     for _ in range(args.steps):
-        fn()
+        g.replay()
     ev[1].record()
     torch.cuda.synchronize()
     assert m.get_status(p) == 0

@@ -93,14 +93,16 @@ __device__ void block_exclusive_scan(const int32_t* in, int n, int32_t* out, int
     }
     if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
-    if (tid == 0) {
-        int32_t run = 0;
-        for (int w = 0; w < PLAN_WARPS; ++w) {
-            const int32_t v = s_warp[w];
-            s_warp[w] = run;
-            run += v;
+    if (warp == 0) {  // exclusive scan of the 16 warp totals
+        const int32_t v = lane < PLAN_WARPS ? s_warp[lane] : 0;
+        int32_t w_incl = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t y = __shfl_up_sync(FULL_MASK, w_incl, off);
+            if (lane >= off) w_incl += y;
         }
-        s_warp[PLAN_WARPS] = run;
+        if (lane < PLAN_WARPS) s_warp[lane] = w_incl - v;
+        if (lane == PLAN_WARPS - 1) s_warp[PLAN_WARPS] = w_incl;
     }
     __syncthreads();
     int32_t run = s_warp[warp] + incl - local;
@@ -153,15 +155,21 @@ __device__ void plan_totals(const PlanArgs& a, const int32_t* s_tot, int32_t* s_
     for (int r = tid; r <= R; r += PLAN_THREADS) a.out.rank_prefix[r] = s_pad[r];
 }
 
-// Per-pair results of a tile's first pass, kept in registers until the slots
-// are known.
-struct TileItems {
-    int e[PLAN_IPT_MAX];     // expert, -1 for an inactive lane
-    int rank[PLAN_IPT_MAX];  // rank among the same expert's pairs of the warp run
-    int ia[PLAN_IPT_MAX];    // group index (group opener) or duplicate position
-    int ib[PLAN_IPT_MAX];    // first duplicate position of the group (opener)
-    int fl[PLAN_IPT_MAX];    // bit 0 duplicate, bit 1 opens a group, bits 2+ duplicates in it
-};
+// Per-pair results of a tile's first pass, kept in shared memory (8 bytes
+// per pair, s_items[warp][step][lane]) until the slots are known, so the
+// item loops stay rolled and the kernels' code stays small (they run once
+// per SM, with a cold instruction cache).
+//   x: expert (11 bits, 0x7ff = inactive lane) | rank among the same
+//      expert's pairs of the warp run (10 bits) | duplicate (1) | opens a
+//      group (1) | duplicates in the group (5)
+//   y: group index (opener) or duplicate position (16) | first duplicate
+//      position of the group (16), both within the warp run
+__device__ __forceinline__ uint2 pack_item(int e, int rank, bool dup, bool opens, int ndup, int ia, int ib) {
+    return make_uint2(static_cast<uint32_t>(e) | (static_cast<uint32_t>(rank) << 11) | (dup ? 1u << 21 : 0u) |
+                          (opens ? 1u << 22 : 0u) | (static_cast<uint32_t>(ndup) << 23),
+                      static_cast<uint32_t>(ia) | (static_cast<uint32_t>(ib) << 16));
+}
+constexpr uint32_t ITEM_NONE = 0x7ffu;
 
 // First pass over a tile: per-warp running counts of every expert (s_wc,
 // [PLAN_WARPS][E], zeroed), each pair's rank among the same expert's pairs
@@ -171,8 +179,8 @@ struct TileItems {
 // is_token_in_rank rows (s_itr, zeroed) and per-warp group / duplicate
 // totals (s_wg, s_wd).  With s_rtok non-null it also counts the tile's
 // tokens per rank.  Reads only topk_idx.
-__device__ __forceinline__ void tile_phase1(const PlanArgs& a, int tile, int32_t* s_wc, uint8_t* s_itr, int32_t* s_wg,
-                                            int32_t* s_wd, int32_t* s_rtok, TileItems& it) {
+__device__ __noinline__ void tile_phase1(const PlanArgs& a, int tile, int32_t* s_wc, uint8_t* s_itr, int32_t* s_wg,
+                                         int32_t* s_wd, int32_t* s_rtok, uint2* s_items) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int E = a.E, K = a.K, R = a.R;
     const int64_t tok0 = static_cast<int64_t>(tile) * a.tile_tokens;
@@ -181,16 +189,25 @@ __device__ __forceinline__ void tile_phase1(const PlanArgs& a, int tile, int32_t
     const int tok_in_iter = lane / K, k = lane - (lane / K) * K;
     const int tok_lane0 = tok_in_iter * K;
     const unsigned below_tok = (1u << tok_lane0) - 1u;
-    int run_g = 0, run_d = 0;
+    // all of this lane's expert ids first: one memory latency for the tile
+    int ids[PLAN_IPT_MAX];
 #pragma unroll
     for (int i = 0; i < PLAN_IPT_MAX; ++i) {
-        it.e[i] = -1;
-        if (i >= a.ipt) continue;
+        const int64_t s = tok0 + static_cast<int64_t>(warp * a.ipt + i) * a.tpw + tok_in_iter;
+        ids[i] = (i < a.ipt && lane < act && s < a.N) ? __ldg(a.topk + s * K + k) : -1;
+    }
+    int run_g = 0, run_d = 0;
+#pragma unroll 1
+    for (int i = 0; i < a.ipt; ++i) {
+        int id = ids[0];
+#pragma unroll
+        for (int q = 1; q < PLAN_IPT_MAX; ++q)
+            if (q == i) id = ids[q];
         const int64_t s = tok0 + static_cast<int64_t>(warp * a.ipt + i) * a.tpw + tok_in_iter;
         bool active = lane < act && s < a.N;
         int e = E;
         if (active) {
-            e = __ldg(a.topk + s * K + k);
+            e = id;
             if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
                 record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(s * K + k));
                 active = false;
@@ -212,27 +229,30 @@ __device__ __forceinline__ void tile_phase1(const PlanArgs& a, int tile, int32_t
         const bool opens = prim && __popc(pd) >= 2;
         const unsigned gball = __ballot_sync(FULL_MASK, opens);
         const unsigned dball = __ballot_sync(FULL_MASK, dup);
-        // duplicates of this token ordered by (primary lane, lane)
+        // Duplicates of a token are laid out group after group (groups in
+        // order of their primary lane = first k), k order inside a group.
+        // A warp scan of the group sizes gives the duplicates of the
+        // token's groups that open before a given lane.
         const int my_p = __ffs(pd) - 1;
-        int before = 0;
-        for (int j = 0; j < K; ++j) {
-            const int lj = (tok_lane0 + j) & 31;
-            const int pj = __shfl_sync(FULL_MASK, my_p, lj);
-            const int dj = __shfl_sync(FULL_MASK, dup ? 1 : 0, lj);
-            if (dj && (pj < my_p || (pj == my_p && lj < lane))) ++before;
+        const int gsz = opens ? __popc(pd) - 1 : 0;
+        int incl = gsz;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(FULL_MASK, incl, off);
+            if (lane >= off) incl += y;
         }
+        const int excl = incl - gsz;
+        const int tok_base = __shfl_sync(FULL_MASK, excl, tok_lane0);
+        const int groups_before = __shfl_sync(FULL_MASK, excl, my_p) - tok_base;
+        const int before = groups_before + (dup ? __popc(pd & lt) - 1 : 0);
         const int dup_pos = run_d + __popc(dball & below_tok) + before;
         if (prim) {
             s_itr[(s - tok0) * R + r] = 1;
             if (s_rtok != nullptr) atomicAdd(&s_rtok[r], 1);
         }
-        if (active) {
-            it.e[i] = e;
-            it.rank[i] = wr;
-            it.fl[i] = (dup ? 1 : 0) | (opens ? 2 : 0) | ((__popc(pd) - 1) << 2);
-            it.ia[i] = opens ? run_g + __popc(gball & lt) : dup_pos;
-            it.ib[i] = dup_pos;
-        }
+        s_items[(warp * a.ipt + i) * 32 + lane] =
+            active ? pack_item(e, wr, dup, opens, __popc(pd) - 1, opens ? run_g + __popc(gball & lt) : dup_pos, dup_pos)
+                   : make_uint2(ITEM_NONE, 0u);
         run_g += __popc(gball);
         run_d += __popc(dball);
     }
@@ -242,13 +262,27 @@ __device__ __forceinline__ void tile_phase1(const PlanArgs& a, int tile, int32_t
     }
 }
 
+// Exclusive scan of 16 per-warp values by one warp (lane w holds warp w's
+// value); returns the base of lane's warp and writes it back.
+__device__ __forceinline__ void warp_scan16(int32_t* s_val, int32_t base) {
+    const int lane = threadIdx.x & 31;
+    int32_t v = lane < PLAN_WARPS ? s_val[lane] : 0;
+    int32_t incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t y = __shfl_up_sync(FULL_MASK, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane < PLAN_WARPS) s_val[lane] = base + incl - v;
+}
+
 // Second pass over a tile, after the bases are known: s_base[e] = first slot
 // of expert e in this tile, g_base / d_base = groups / duplicates of earlier
 // tiles.  Turns the per-warp counts into per-warp bases, then writes dst,
 // src_of_slot, dup_groups, dup_loffs and the tile's is_token_in_rank rows.
-__device__ __forceinline__ void tile_phase3(const PlanArgs& a, int tile, const int32_t* s_base, int32_t g_base,
-                                            int32_t d_base, int32_t* s_wc, int32_t* s_wg, int32_t* s_wd,
-                                            const uint8_t* s_itr, const TileItems& it) {
+__device__ __noinline__ void tile_phase3(const PlanArgs& a, int tile, const int32_t* s_base, int32_t g_base,
+                                         int32_t d_base, int32_t* s_wc, int32_t* s_wg, int32_t* s_wd,
+                                         const uint8_t* s_itr, const uint2* s_items) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int E = a.E, K = a.K, R = a.R;
     const int64_t tok0 = static_cast<int64_t>(tile) * a.tile_tokens;
@@ -261,45 +295,41 @@ __device__ __forceinline__ void tile_phase3(const PlanArgs& a, int tile, const i
             run += v;
         }
     }
-    if (tid == 0) {
-        int32_t g = g_base, d = d_base;
-        for (int w = 0; w < PLAN_WARPS; ++w) {
-            const int32_t vg = s_wg[w], vd = s_wd[w];
-            s_wg[w] = g;
-            s_wd[w] = d;
-            g += vg;
-            d += vd;
-        }
-    }
+    if (warp == PLAN_WARPS - 1) warp_scan16(s_wg, g_base);
+    if (warp == PLAN_WARPS - 2) warp_scan16(s_wd, d_base);
     __syncthreads();
 
     const int tok_in_iter = lane / K, k = lane - (lane / K) * K;
-#pragma unroll
-    for (int i = 0; i < PLAN_IPT_MAX; ++i) {
-        if (it.e[i] < 0) continue;
-        const int e = it.e[i];
+    const int32_t wg = s_wg[warp], wd = s_wd[warp];
+#pragma unroll 1
+    for (int i = 0; i < a.ipt; ++i) {
+        const uint2 it = s_items[(warp * a.ipt + i) * 32 + lane];
+        const uint32_t e = it.x & 0x7ffu;
+        if (e == ITEM_NONE) continue;
         const int64_t s = tok0 + static_cast<int64_t>(warp * a.ipt + i) * a.tpw + tok_in_iter;
         const int64_t f = s * K + k;
-        const int32_t slot = s_wc[warp * E + e] + it.rank[i];
+        const int32_t slot = s_wc[warp * E + e] + static_cast<int32_t>((it.x >> 11) & 0x3ffu);
         if (slot < 0 || static_cast<int64_t>(slot) >= a.p_cap) {
             record_error(a.out.status, MOE_ERR_DEVICE_INDEX, slot);
             continue;
         }
-        const bool dup = it.fl[i] & 1;
+        const bool dup = (it.x >> 21) & 1u;
+        const bool opens = (it.x >> 22) & 1u;
+        const int32_t ia = static_cast<int32_t>(it.y & 0xffffu), ib = static_cast<int32_t>(it.y >> 16);
         a.out.dst[f] = dup ? -slot - 1 : slot;
         a.out.src_of_slot[slot] = static_cast<int32_t>(f);
-        if (it.fl[i] & 2) {
-            const int64_t g = static_cast<int64_t>(s_wg[warp]) + it.ia[i];
+        if (opens) {
+            const int64_t g = static_cast<int64_t>(wg) + ia;
             if (g >= static_cast<int64_t>(a.N) * (K / 2)) {
                 record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(g));
                 continue;
             }
             int32_t* row = a.out.dup_groups + 3 * g;
             row[0] = slot;
-            row[1] = s_wd[warp] + it.ib[i];
-            row[2] = it.fl[i] >> 2;
+            row[1] = wd + ib;
+            row[2] = static_cast<int32_t>(it.x >> 23);
         } else if (dup) {
-            const int64_t pos = static_cast<int64_t>(s_wd[warp]) + it.ia[i];
+            const int64_t pos = static_cast<int64_t>(wd) + ia;
             if (pos >= static_cast<int64_t>(a.N) * (K - 1)) {
                 record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(pos));
                 continue;
@@ -489,7 +519,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_count_kernel(const PlanArgs
 // ---------------------------------------------------------------- launch 2
 __global__ void __launch_bounds__(PLAN_THREADS) plan_scatter_kernel(const PlanArgs a) {
     extern __shared__ __align__(16) int32_t s_dyn[];
-    int32_t* s_wc = s_dyn;                                             // [PLAN_WARPS][E]
+    uint2* s_items = reinterpret_cast<uint2*>(s_dyn);                  // [PLAN_WARPS][ipt][32]
+    int32_t* s_wc = s_dyn + 2 * PLAN_WARPS * 32 * a.ipt;               // [PLAN_WARPS][E]
     int32_t* s_base = s_wc + PLAN_WARPS * a.E;                         // [E]
     uint8_t* s_itr = reinterpret_cast<uint8_t*>(s_base + a.E);         // [tile_tokens][R]
     __shared__ int32_t s_wg[PLAN_WARPS], s_wd[PLAN_WARPS];
@@ -504,8 +535,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_scatter_kernel(const PlanAr
     __syncthreads();
 
     // Reads only topk_idx, which was complete before launch 1 passed its wait.
-    TileItems it;
-    tile_phase1(a, tile, s_wc, s_itr, s_wg, s_wd, nullptr, it);
+    tile_phase1(a, tile, s_wc, s_itr, s_wg, s_wd, nullptr, s_items);
 
     // ---- everything below needs launch 1's outputs
     pdl_wait();
@@ -517,7 +547,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_scatter_kernel(const PlanAr
     for (int e = tid; e < E; e += PLAN_THREADS) s_base[e] = __ldg(a.out.cu_seqlens + e) + __ldg(tp + e);
     const int32_t g_base = __ldg(tp + E + R), d_base = __ldg(tp + E + R + 1);
     __syncthreads();
-    tile_phase3(a, tile, s_base, g_base, d_base, s_wc, s_wg, s_wd, s_itr, it);
+    tile_phase3(a, tile, s_base, g_base, d_base, s_wc, s_wg, s_wd, s_itr, s_items);
     fill_unused(a, tile, a.T, a.out.cu_seqlens, a.out.tokens_per_expert);
 }
 
@@ -557,7 +587,8 @@ __device__ __forceinline__ int32_t ld_dsmem_s32(uint32_t addr) {
 __global__ void __launch_bounds__(PLAN_THREADS) plan_cluster_kernel(const PlanArgs a) {
     extern __shared__ __align__(16) int32_t s_dyn[];
     const int E = a.E, R = a.R, C = a.C;
-    int32_t* s_wc = s_dyn;                        // [PLAN_WARPS][E]
+    uint2* s_items = reinterpret_cast<uint2*>(s_dyn);  // [PLAN_WARPS][ipt][32]
+    int32_t* s_wc = s_dyn + 2 * PLAN_WARPS * 32 * a.ipt;  // [PLAN_WARPS][E]
     int32_t* s_cnt = s_wc + PLAN_WARPS * E;       // [C]  this tile's column counts
     int32_t* s_tot = s_cnt + C;                   // [C]  cluster totals
     int32_t* s_base = s_tot + C;                  // [E]
@@ -579,8 +610,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_cluster_kernel(const PlanAr
     for (int c = E + tid; c < C; c += PLAN_THREADS) s_cnt[c] = 0;
     __syncthreads();
 
-    TileItems it;
-    tile_phase1(a, tile, s_wc, s_itr, s_wg, s_wd, s_cnt + E, it);
+    tile_phase1(a, tile, s_wc, s_itr, s_wg, s_wd, s_cnt + E, s_items);
     __syncthreads();
     for (int e = tid; e < E; e += PLAN_THREADS) {
         int32_t c = 0;
@@ -601,11 +631,14 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_cluster_kernel(const PlanAr
     cluster_wait();
 
     for (int c = tid; c < C; c += PLAN_THREADS) {
+        int32_t v[16];
+#pragma unroll
+        for (uint32_t q = 0; q < 16; ++q) v[q] = q < ncta ? ld_dsmem_s32(dsmem_addr(s_cnt + c, q)) : 0;
         int32_t excl = 0, tot = 0;
-        for (uint32_t q = 0; q < ncta; ++q) {
-            const int32_t v = ld_dsmem_s32(dsmem_addr(s_cnt + c, q));
-            if (q < rank) excl += v;
-            tot += v;
+#pragma unroll
+        for (uint32_t q = 0; q < 16; ++q) {
+            if (q < rank) excl += v[q];
+            tot += v[q];
         }
         s_tot[c] = tot;
         if (c < E) s_base[c] = excl;
@@ -618,7 +651,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_cluster_kernel(const PlanAr
     plan_totals(a, s_tot, s_pad, s_cu, s_warp, rank == 0);
     for (int e = tid; e < E; e += PLAN_THREADS) s_base[e] += s_cu[e];
     __syncthreads();
-    tile_phase3(a, tile, s_base, s_gd[0], s_gd[1], s_wc, s_wg, s_wd, s_itr, it);
+    tile_phase3(a, tile, s_base, s_gd[0], s_gd[1], s_wc, s_wg, s_wd, s_itr, s_items);
     fill_unused(a, tile, static_cast<int>(ncta), s_cu, s_tot);
     cluster_wait();  // keep this CTA's shared memory alive until all reads are done
 }
@@ -701,8 +734,8 @@ bool cluster_geometry(int N, int E, int K, int R, Geom* g) {
 }
 
 size_t cluster_smem(const Geom& g, int E, int R) {
-    const size_t ints = static_cast<size_t>(moe::PLAN_WARPS) * E + 2 * static_cast<size_t>(g.C) + E +
-                        2 * static_cast<size_t>(E + R + 2);
+    const size_t ints = static_cast<size_t>(2 * moe::PLAN_WARPS * 32) * g.ipt + static_cast<size_t>(moe::PLAN_WARPS) * E +
+                        2 * static_cast<size_t>(g.C) + E + 2 * static_cast<size_t>(E + R + 2);
     return sizeof(int32_t) * ints + (static_cast<size_t>(g.tile_tokens) * R + 15) / 16 * 16;
 }
 
@@ -849,7 +882,8 @@ extern "C" MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, in
 
     // ---- two launches: decoupled look-back over tiles, then the scatter
     const size_t smem1 = sizeof(int32_t) * (static_cast<size_t>(g.C) + 2 * (E + R + 2) + 2);
-    const size_t smem2 = sizeof(int32_t) * static_cast<size_t>(moe::PLAN_WARPS + 1) * E +
+    const size_t smem2 = sizeof(int32_t) * (static_cast<size_t>(moe::PLAN_WARPS + 1) * E +
+                                            static_cast<size_t>(2 * moe::PLAN_WARPS * 32) * g.ipt) +
                          (static_cast<size_t>(g.tile_tokens) * R + 15) / 16 * 16;
     rc = moe_host::launch(moe::plan_count_kernel, dim3(g.T), dim3(moe::PLAN_THREADS), smem1, stream, a);
     if (rc != MOE_OK) return rc;

@@ -81,6 +81,29 @@ __device__ __forceinline__ float exp_diff(float a, float b) {
     return __fmaf_rn(e, err, e);
 }
 
+// Float-float accumulation (hi + lo, |lo| <= ulp(hi)/2) of non-negative
+// terms: TwoSum of the heads, tails added, Fast2Sum renormalisation.
+__device__ __forceinline__ void ff_add(float& hi, float& lo, float bh, float bl) {
+    const float s = __fadd_rn(hi, bh);
+    const float bb = __fsub_rn(s, hi);
+    const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(bh, bb));
+    const float t = __fadd_rn(__fadd_rn(lo, bl), err);
+    hi = __fadd_rn(s, t);
+    lo = __fsub_rn(t, __fsub_rn(hi, s));
+}
+
+// A winner's score for its weight: the same 1/(1+e^-x) (x >= 0) or
+// e^x/(1+e^x) as the key, with the rounding error of 1+e carried to first
+// order, so only e's own error (about 1 ulp) and two roundings remain.
+__device__ __forceinline__ float sigmoid_weight(float x) {
+    const bool pos = x >= 0.0f;
+    const float e = exp_nonpos(pos ? -x : x);
+    const float d = __fadd_rn(1.0f, e);
+    const float dlo = __fsub_rn(e, __fsub_rn(d, 1.0f));  // exact: 1 + e = d + dlo
+    const float q = __fdiv_rn(pos ? 1.0f : e, d);
+    return __fmaf_rn(-q, __fdiv_rn(dlo, d), q);
+}
+
 struct RouteArgs {
     const float* logits;
     const float* bias;
@@ -103,49 +126,65 @@ __device__ __forceinline__ int expert_of(int sub, int v) {
     }
 }
 
+template <int G, int V, bool VEC>
+__device__ __forceinline__ void load_row(const RouteArgs& a, int64_t s, int sub, float (&raw)[V]) {
+    const bool valid = s < a.N;
+    const float* row = a.logits + (valid ? s : 0) * a.E;
+    if constexpr (VEC) {
+#pragma unroll
+        for (int j = 0; j < V / 4; ++j) {
+            const int e0 = 4 * (sub + G * j);
+            float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (valid && e0 < a.E) q = ld_stream_f4(row + e0);
+            raw[4 * j + 0] = q.x;
+            raw[4 * j + 1] = q.y;
+            raw[4 * j + 2] = q.z;
+            raw[4 * j + 3] = q.w;
+        }
+    } else {
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const int e = sub + G * v;
+            raw[v] = (valid && e < a.E) ? ld_stream_f32(row + e) : 0.f;
+        }
+    }
+}
+
 template <int G, int V, bool VEC, int KMAX>
 __global__ void __launch_bounds__(ROUTE_THREADS) route_topk_kernel(const RouteArgs a) {
-    extern __shared__ float s_keys_all[];  // [warps][E], group-limited only
+    extern __shared__ float s_keys_all[];  // [warps][E], general group-limited path only
     pdl_wait();
     pdl_trigger();
 
+    constexpr int TPW = 32 / G;                  // tokens per warp
+    constexpr int KPL = (KMAX + G - 1) / G;      // winners kept per lane
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int sub = lane % G;
-    const int group_base = lane - sub;
-    constexpr int TPW = 32 / G;  // tokens per warp
     const int E = a.E, K = a.K;
     const bool sigmoid = a.scoring == MOE_SCORING_SIGMOID;
+    const bool grouped = a.n_group > 1;
+    const int gs = E / a.n_group;
+    // Register path for group scores: a group is a run of L = gs/4 lanes
+    // of one float4 slot (needs G = 32, float4 rows, L a power of two).
+    const int L = gs / 4;
+    const bool gfast = G == 32 && VEC && grouped && gs % 4 == 0 && L >= 1 && L <= 32 && (L & (L - 1)) == 0;
     float* s_keys = s_keys_all + warp * E;
 
-    const int64_t warps_total = static_cast<int64_t>(gridDim.x) * (ROUTE_THREADS / 32);
-    for (int64_t wtok = (static_cast<int64_t>(blockIdx.x) * (ROUTE_THREADS / 32) + warp) * TPW;
-         wtok < a.N; wtok += warps_total * TPW) {
+    const int64_t step = static_cast<int64_t>(gridDim.x) * (ROUTE_THREADS / 32) * TPW;
+    int64_t wtok = (static_cast<int64_t>(blockIdx.x) * (ROUTE_THREADS / 32) + warp) * TPW;
+    float nxt[V];
+    if (wtok < a.N) load_row<G, V, VEC>(a, wtok + lane / G, sub, nxt);
+    for (; wtok < a.N; wtok += step) {
         const int64_t s = wtok + lane / G;
         const bool valid = s < a.N;
-        const float* row = a.logits + (valid ? s : 0) * E;
+        float raw[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) raw[v] = nxt[v];
+        if (wtok + step < a.N) load_row<G, V, VEC>(a, wtok + step + lane / G, sub, nxt);  // next token in flight
 
-        // ---- load and score
-        float raw[V];  // logits
+        // ---- keys
         float keyf[V];
-        if constexpr (VEC) {
-#pragma unroll
-            for (int j = 0; j < V / 4; ++j) {
-                const int e0 = 4 * (sub + G * j);
-                float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (valid && e0 < E) q = ld_stream_f4(row + e0);
-                raw[4 * j + 0] = q.x;
-                raw[4 * j + 1] = q.y;
-                raw[4 * j + 2] = q.z;
-                raw[4 * j + 3] = q.w;
-            }
-        } else {
-#pragma unroll
-            for (int v = 0; v < V; ++v) {
-                const int e = sub + G * v;
-                raw[v] = (valid && e < E) ? ld_stream_f32(row + e) : 0.f;
-            }
-        }
         uint32_t key[V];
 #pragma unroll
         for (int v = 0; v < V; ++v) {
@@ -159,62 +198,110 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_topk_kernel(const RouteAr
             key[v] = (valid && e < E) ? order_key(keyf[v]) : 0u;
         }
 
-        // ---- group-limited eligibility (G == 32 only; host enforces)
+        // ---- group-limited eligibility
         if constexpr (G == 32) {
-            if (a.n_group > 1) {
-#pragma unroll
-                for (int v = 0; v < V; ++v) {
-                    const int e = expert_of<G, V, VEC>(sub, v);
-                    if (e < E) s_keys[e] = keyf[v];
-                }
-                __syncwarp();
-                const int gs = E / a.n_group;
-                uint32_t gkey = 0u;
-                if (lane < a.n_group) {
-                    float m1 = -INFINITY, m2 = -INFINITY;
-                    for (int j = 0; j < gs; ++j) {
-                        const float x = s_keys[lane * gs + j];
-                        if (x > m1) {
-                            m2 = m1;
-                            m1 = x;
-                        } else if (x > m2) {
-                            m2 = x;
-                        }
-                    }
-                    gkey = order_key(gs == 1 ? m1 : __fadd_rn(m1, m2));
-                }
+            if (grouped) {
                 uint32_t kept = 0u;
-                for (int r = 0; r < a.topk_group; ++r) {
-                    const uint32_t m = __reduce_max_sync(FULL_MASK, gkey);
-                    const uint32_t win = __reduce_min_sync(FULL_MASK, gkey == m ? static_cast<uint32_t>(lane) : 32u);
-                    kept |= 1u << win;
-                    if (static_cast<uint32_t>(lane) == win) gkey = 0u;
-                }
+                if (gfast) {
+                    // top-2 of each lane's float4, merged over the group's lanes
+                    float sc[V / 4 > 0 ? V / 4 : 1];
 #pragma unroll
-                for (int v = 0; v < V; ++v) {
-                    const int e = expert_of<G, V, VEC>(sub, v);
-                    if (e < E && !((kept >> (e / gs)) & 1u)) key[v] = 0u;
+                    for (int j = 0; j < V / 4; ++j) {
+                        const float x0 = keyf[4 * j], x1 = keyf[4 * j + 1], x2 = keyf[4 * j + 2], x3 = keyf[4 * j + 3];
+                        const float hi01 = fmaxf(x0, x1), lo01 = fminf(x0, x1);
+                        const float hi23 = fmaxf(x2, x3), lo23 = fminf(x2, x3);
+                        float m1 = fmaxf(hi01, hi23);
+                        float m2 = fmaxf(fminf(hi01, hi23), fmaxf(lo01, lo23));
+                        for (int off = 1; off < L; off <<= 1) {
+                            const float o1 = __shfl_xor_sync(FULL_MASK, m1, off);
+                            const float o2 = __shfl_xor_sync(FULL_MASK, m2, off);
+                            const float n1 = fmaxf(m1, o1);
+                            m2 = fmaxf(fminf(m1, o1), fmaxf(m2, o2));
+                            m1 = n1;
+                        }
+                        sc[j] = __fadd_rn(m1, m2);
+                    }
+                    const int gpj = 32 / L;  // groups per float4 slot
+                    uint32_t taken = 0u;     // candidate slots of this lane already kept
+                    for (int r = 0; r < a.topk_group; ++r) {
+                        uint32_t ck = 0u, cg = 32u;
+#pragma unroll
+                        for (int j = 0; j < V / 4; ++j) {
+                            const int g = j * gpj + lane / L;
+                            const bool cand = (lane % L) == 0 && g < a.n_group && !((taken >> j) & 1u);
+                            const uint32_t k2 = cand ? order_key(sc[j]) : 0u;
+                            if (k2 > ck) {
+                                ck = k2;
+                                cg = static_cast<uint32_t>(g);
+                            }
+                        }
+                        const uint32_t m = __reduce_max_sync(FULL_MASK, ck);
+                        const uint32_t win = __reduce_min_sync(FULL_MASK, ck == m ? cg : 32u);
+                        kept |= 1u << win;
+#pragma unroll
+                        for (int j = 0; j < V / 4; ++j)
+                            if ((lane % L) == 0 && static_cast<uint32_t>(j * gpj + lane / L) == win) taken |= 1u << j;
+                    }
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        const int g = (v / 4) * gpj + lane / L;
+                        if (!((kept >> g) & 1u)) key[v] = 0u;
+                    }
+                } else {
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        const int e = expert_of<G, V, VEC>(sub, v);
+                        if (e < E) s_keys[e] = keyf[v];
+                    }
+                    __syncwarp();
+                    uint32_t gkey = 0u;
+                    if (lane < a.n_group) {
+                        float m1 = -INFINITY, m2 = -INFINITY;
+                        for (int j = 0; j < gs; ++j) {
+                            const float x = s_keys[lane * gs + j];
+                            if (x > m1) {
+                                m2 = m1;
+                                m1 = x;
+                            } else if (x > m2) {
+                                m2 = x;
+                            }
+                        }
+                        gkey = order_key(gs == 1 ? m1 : __fadd_rn(m1, m2));
+                    }
+                    for (int r = 0; r < a.topk_group; ++r) {
+                        const uint32_t m = __reduce_max_sync(FULL_MASK, gkey);
+                        const uint32_t win =
+                            __reduce_min_sync(FULL_MASK, gkey == m ? static_cast<uint32_t>(lane) : 32u);
+                        kept |= 1u << win;
+                        if (static_cast<uint32_t>(lane) == win) gkey = 0u;
+                    }
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        const int e = expert_of<G, V, VEC>(sub, v);
+                        if (e < E && !((kept >> (e / gs)) & 1u)) key[v] = 0u;
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
             }
         }
 
-        // ---- K rounds of arg-max
-        int win_idx[KMAX];
-        float win_val[KMAX];
+        // ---- K rounds of arg-max; each lane keeps its best and rescans only
+        // when its best wins
+        uint32_t bk = 0u, bi = 0xffffffffu;
+        float bv = 0.f;
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+            if (key[v] > bk) {  // values ascend in expert index per lane
+                bk = key[v];
+                bi = static_cast<uint32_t>(expert_of<G, V, VEC>(sub, v));
+                bv = raw[v];
+            }
+        int my_idx[KPL];
+        float my_val[KPL];
+        float top_val = 0.f;
 #pragma unroll
         for (int r = 0; r < KMAX; ++r) {
             if (r >= K) break;
-            uint32_t bk = 0u, bi = 0xffffffffu;
-            float bv = 0.f;
-#pragma unroll
-            for (int v = 0; v < V; ++v) {
-                if (key[v] > bk) {  // values ascend in expert index per lane
-                    bk = key[v];
-                    bi = static_cast<uint32_t>(expert_of<G, V, VEC>(sub, v));
-                    bv = raw[v];
-                }
-            }
             uint32_t wi;
             float wv;
             if constexpr (G == 32) {
@@ -223,95 +310,123 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_topk_kernel(const RouteAr
                 const int owner = VEC ? static_cast<int>((wi / 4) % G) : static_cast<int>(wi % G);
                 wv = __shfl_sync(FULL_MASK, bv, owner);
             } else {
+                uint32_t ck = bk, ci = bi;
+                float cv = bv;
 #pragma unroll
                 for (int off = 1; off < G; off <<= 1) {
-                    const uint32_t ok = __shfl_xor_sync(FULL_MASK, bk, off);
-                    const uint32_t oi = __shfl_xor_sync(FULL_MASK, bi, off);
-                    const float ov = __shfl_xor_sync(FULL_MASK, bv, off);
-                    if (ok > bk || (ok == bk && oi < bi)) {
-                        bk = ok;
-                        bi = oi;
-                        bv = ov;
+                    const uint32_t ok = __shfl_xor_sync(FULL_MASK, ck, off);
+                    const uint32_t oi = __shfl_xor_sync(FULL_MASK, ci, off);
+                    const float ov = __shfl_xor_sync(FULL_MASK, cv, off);
+                    if (ok > ck || (ok == ck && oi < ci)) {
+                        ck = ok;
+                        ci = oi;
+                        cv = ov;
                     }
                 }
-                wi = bi;
-                wv = bv;
+                wi = ci;
+                wv = cv;
             }
+            if (bi == wi) {  // this lane owned the winner: drop it, find its next best
+#pragma unroll
+                for (int v = 0; v < V; ++v)
+                    if (static_cast<uint32_t>(expert_of<G, V, VEC>(sub, v)) == wi) key[v] = 0u;
+                bk = 0u;
+                bi = 0xffffffffu;
+#pragma unroll
+                for (int v = 0; v < V; ++v)
+                    if (key[v] > bk) {
+                        bk = key[v];
+                        bi = static_cast<uint32_t>(expert_of<G, V, VEC>(sub, v));
+                        bv = raw[v];
+                    }
+            }
+            if (r == 0) top_val = wv;
+            if (r % G == sub) {
+                my_idx[r / G] = static_cast<int>(wi);
+                my_val[r / G] = wv;
+            }
+        }
+
+        // ---- weights: lane `sub` owns winners k = sub, sub + G, ...
+        float num[KPL];
+        float shi = 0.f, slo = 0.f;  // this lane's part of the normaliser
+#pragma unroll
+        for (int t = 0; t < KPL; ++t) {
+            const int k = sub + G * t;
+            num[t] = 0.f;
+            if (k >= K) continue;
+            if (!sigmoid) {
+                num[t] = exp_diff(my_val[t], top_val);  // top-1 logit is the row maximum
+            } else {
+                num[t] = sigmoid_weight(my_val[t]);
+            }
+            if (a.renormalize && (!sigmoid || num[t] >= 0x1p-100f)) ff_add(shi, slo, num[t], 0.f);
+        }
+        if (!sigmoid && !a.renormalize) {  // full-row softmax normaliser
+            shi = 0.f;
+            slo = 0.f;
 #pragma unroll
             for (int v = 0; v < V; ++v) {
-                if (static_cast<uint32_t>(expert_of<G, V, VEC>(sub, v)) == wi) key[v] = 0u;
+                const int e = expert_of<G, V, VEC>(sub, v);
+                if (valid && e < E) ff_add(shi, slo, exp_diff(raw[v], top_val), 0.f);
             }
-            win_idx[r] = static_cast<int>(wi);
-            win_val[r] = wv;
         }
-
-        // ---- weights (win_val holds the winners' logits)
-        float w[KMAX];
-        if (!sigmoid) {
-            const float m = win_val[0];  // top-1 logit is the row maximum
-            float ek[KMAX];
-            double denom = 0.0;
+        bool tiny = false;  // a sigmoid score below 2^-100: fp64 for this token
+        if (sigmoid) {
 #pragma unroll
-            for (int r = 0; r < KMAX; ++r) {
-                if (r >= K) break;
-                ek[r] = exp_diff(win_val[r], m);
-                denom += static_cast<double>(ek[r]);
-            }
-            if (!a.renormalize) {
-                double part = 0.0;
+            for (int t = 0; t < KPL; ++t)
+                if (sub + G * t < K && num[t] < 0x1p-100f) tiny = true;
+        }
+        if (__any_sync(FULL_MASK, tiny)) {
+            // rare: recompute the warp's scores and normalisers in fp64
+            // (the reduction stays inside each token's group of G lanes)
+            double sd[KPL], den = 0.0;
 #pragma unroll
-                for (int v = 0; v < V; ++v) {
-                    const int e = expert_of<G, V, VEC>(sub, v);
-                    if (valid && e < E) part += static_cast<double>(exp_diff(raw[v], m));
+            for (int t = 0; t < KPL; ++t) {
+                const int k = sub + G * t;
+                sd[t] = 0.0;
+                if (k < K) {
+                    const double ex = exp(-fabs(static_cast<double>(my_val[t])));
+                    sd[t] = my_val[t] >= 0.f ? 1.0 / (1.0 + ex) : ex / (1.0 + ex);
                 }
-#pragma unroll
-                for (int off = 1; off < G; off <<= 1) part += __shfl_xor_sync(FULL_MASK, part, off);
-                denom = part;
+                den += sd[t];
             }
-            const double scale = static_cast<double>(a.scaling) / denom;
 #pragma unroll
-            for (int r = 0; r < KMAX; ++r) {
-                if (r >= K) break;
-                w[r] = static_cast<float>(static_cast<double>(ek[r]) * scale);
-            }
+            for (int off = 1; off < G; off <<= 1) den += __shfl_xor_sync(FULL_MASK, den, off);
+            const double scale = a.renormalize ? static_cast<double>(a.scaling) / den : a.scaling;
+#pragma unroll
+            for (int t = 0; t < KPL; ++t) num[t] = static_cast<float>(sd[t] * scale);
         } else {
-            // scores of the winners; below 2^-100 the fp32 score has lost
-            // relative precision (or underflowed), so fp64 takes over there
-            double sc[KMAX];
-            double denom = 0.0;
 #pragma unroll
-            for (int r = 0; r < KMAX; ++r) {
-                if (r >= K) break;
-                const float sf = sigmoid_f32(win_val[r]);
-                if (sf < 0x1p-100f) {
-                    const double ex = exp(static_cast<double>(win_val[r]));
-                    sc[r] = ex / (1.0 + ex);
-                } else {
-                    sc[r] = static_cast<double>(sf);
-                }
-                denom += sc[r];
+            for (int off = 1; off < G; off <<= 1) {
+                const float oh = __shfl_xor_sync(FULL_MASK, shi, off);
+                const float ol = __shfl_xor_sync(FULL_MASK, slo, off);
+                ff_add(shi, slo, oh, ol);
             }
-            const double scale = a.renormalize ? static_cast<double>(a.scaling) / denom
-                                               : static_cast<double>(a.scaling);
+            if (a.renormalize || !sigmoid) {
+                // w = num * scaling / (shi + slo): one correctly rounded
+                // division, then the tail of the normaliser to first order
+                const float q = __fdiv_rn(a.scaling, shi);
+                const float qc = __fmaf_rn(-q, __fdiv_rn(slo, shi), q);
 #pragma unroll
-            for (int r = 0; r < KMAX; ++r) {
-                if (r >= K) break;
-                w[r] = static_cast<float>(sc[r] * scale);
+                for (int t = 0; t < KPL; ++t) num[t] = __fmul_rn(num[t], qc);
+            } else {
+#pragma unroll
+                for (int t = 0; t < KPL; ++t) num[t] = __fmul_rn(num[t], a.scaling);
             }
         }
 
-        // ---- store: lane `sub` writes k = sub, sub + G, ...
+        // ---- store
         if (valid) {
 #pragma unroll
-            for (int r = 0; r < KMAX; ++r) {
-                if (r >= K) break;
-                if (r % G == sub) {
-                    a.topk_idx[s * K + r] = win_idx[r];
-                    a.topk_w[s * K + r] = w[r];
+            for (int t = 0; t < KPL; ++t) {
+                const int k = sub + G * t;
+                if (k < K) {
+                    a.topk_idx[s * K + k] = my_idx[t];
+                    a.topk_w[s * K + k] = num[t];
                 }
             }
         }
-        (void)group_base;
     }
 }
 

@@ -317,6 +317,9 @@ extern "C" MOE_API int moe_permute(const uint16_t* x, int N, int H, int K, int E
     int64_t G = target / row_bytes;
     if (G < 1) G = 1;
     if (G > 64) G = 64;
+    // small batches: at least two groups per SM so every SM moves rows
+    const int64_t spread = (static_cast<int64_t>(N) + 2 * moe_host::num_sms() - 1) / (2 * moe_host::num_sms());
+    if (G > spread) G = spread < 1 ? 1 : spread;
     if (G > N) G = N;
     a.G = static_cast<int>(G);
     a.stage_bytes = static_cast<uint32_t>((G * row_bytes + 127) / 128 * 128);
@@ -331,13 +334,19 @@ extern "C" MOE_API int moe_permute(const uint16_t* x, int N, int H, int K, int E
     a.slots_bytes = slots_for(stages);
     a.n_groups = (N + G - 1) / G;
     a.timeout_ns = moe_host::timeout_ns();
-    const size_t smem = 128 + a.slots_bytes + static_cast<size_t>(stages) * a.stage_bytes;
-    if (smem > kSmemPerSm) return MOE_ERR_UNSUPPORTED;
+    if (128 + a.slots_bytes + static_cast<size_t>(stages) * a.stage_bytes > kSmemPerSm) return MOE_ERR_UNSUPPORTED;
     int per_sm = env_int("MOE_PERMUTE_CTAS_PER_SM", 6);
     if (per_sm < 1) per_sm = 1;
     if (per_sm > 16) per_sm = 16;
     int64_t grid = static_cast<int64_t>(moe_host::num_sms()) * per_sm;
     if (grid > a.n_groups) grid = a.n_groups;
+    // no deeper ring than the groups a CTA gets: smaller CTAs, more of them resident
+    const int64_t per_cta = (a.n_groups + grid - 1) / grid;
+    if (per_cta < a.stages) {
+        a.stages = static_cast<int>(per_cta < 2 ? 2 : per_cta);
+        a.slots_bytes = slots_for(a.stages);
+    }
+    const size_t smem = 128 + a.slots_bytes + static_cast<size_t>(a.stages) * a.stage_bytes;
     if (cudaFuncSetAttribute(moe::permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemPerSm)) != cudaSuccess)
         return MOE_ERR_CUDA;
