@@ -61,6 +61,7 @@ struct PlanArgs {
     uint64_t* flags;       // [T][C]
     int32_t* tile_prefix;  // [T][C]
     int N, E, K, R, epn, alignment;
+    uint64_t epn_magic;  // floor(2^32 / epn) + 1: e / epn == (e * epn_magic) >> 32 for e < 2048
     int tpw, ipt, tile_tokens, T, C;
     int64_t p_cap;
     int skip_tile;
@@ -72,6 +73,11 @@ struct PlanArgs {
 // workspace by calls of other sizes are below 2^30, so no leftover word can
 // carry the tag of the running call.
 __device__ __forceinline__ uint32_t flag_tag(uint32_t epoch) { return epoch | 0x80000000u; }
+// Rank of expert e (e < 2048) without an integer division.
+__device__ __forceinline__ int rank_of(const PlanArgs& a, int e) {
+    return static_cast<int>((static_cast<uint64_t>(static_cast<uint32_t>(e)) * a.epn_magic) >> 32);
+}
+
 __device__ __forceinline__ uint64_t pack_flag(uint32_t epoch, uint32_t st, uint32_t v) {
     return (static_cast<uint64_t>(flag_tag(epoch)) << 32) | (static_cast<uint64_t>(st) << 30) | (v & 0x3fffffffu);
 }
@@ -221,7 +227,7 @@ __device__ __noinline__ void tile_phase1(const PlanArgs& a, int tile, int32_t* s
         if (active && (peers & lt) == 0u) s_wc[warp * E + e] = base + __popc(peers);
         __syncwarp();
 
-        const int r = active ? e / a.epn : 0;
+        const int r = active ? rank_of(a, e) : 0;
         const unsigned key = active ? static_cast<unsigned>(tok_in_iter * 128 + r) : 0xffffffffu;
         const unsigned pd = __match_any_sync(FULL_MASK, key);
         const bool prim = active && (pd & lt) == 0u;
@@ -419,7 +425,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_count_kernel(const PlanArgs
             }
             const unsigned peers = __match_any_sync(FULL_MASK, e);
             if (active && (peers & lt) == 0u) atomicAdd(&s_tot[e], __popc(peers));
-            const int r = active ? e / a.epn : 0;
+            const int r = active ? rank_of(a, e) : 0;
             const unsigned key = active ? static_cast<unsigned>(tok_in_iter * 128 + r) : 0xffffffffu;
             const unsigned pd = __match_any_sync(FULL_MASK, key);
             const bool prim = active && (pd & lt) == 0u;
@@ -846,6 +852,7 @@ extern "C" MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, in
     a.K = K;
     a.R = R;
     a.epn = E / R;
+    a.epn_magic = (uint64_t(1) << 32) / static_cast<uint64_t>(a.epn) + 1;
     a.alignment = alignment;
     a.tpw = g.tpw;
     a.ipt = g.ipt;

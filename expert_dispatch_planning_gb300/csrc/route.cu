@@ -221,14 +221,17 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_topk_kernel(const RouteAr
                         }
                         sc[j] = __fadd_rn(m1, m2);
                     }
-                    const int gpj = 32 / L;  // groups per float4 slot
+                    const int lsh = __ffs(L) - 1;        // L is a power of two
+                    const int gpj = 32 >> lsh;           // groups per float4 slot
+                    const int lgrp = lane >> lsh;        // this lane's group within a slot
+                    const bool lead = (lane & (L - 1)) == 0;
                     uint32_t taken = 0u;     // candidate slots of this lane already kept
                     for (int r = 0; r < a.topk_group; ++r) {
                         uint32_t ck = 0u, cg = 32u;
 #pragma unroll
                         for (int j = 0; j < V / 4; ++j) {
-                            const int g = j * gpj + lane / L;
-                            const bool cand = (lane % L) == 0 && g < a.n_group && !((taken >> j) & 1u);
+                            const int g = j * gpj + lgrp;
+                            const bool cand = lead && g < a.n_group && !((taken >> j) & 1u);
                             const uint32_t k2 = cand ? order_key(sc[j]) : 0u;
                             if (k2 > ck) {
                                 ck = k2;
@@ -240,11 +243,11 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_topk_kernel(const RouteAr
                         kept |= 1u << win;
 #pragma unroll
                         for (int j = 0; j < V / 4; ++j)
-                            if ((lane % L) == 0 && static_cast<uint32_t>(j * gpj + lane / L) == win) taken |= 1u << j;
+                            if (lead && static_cast<uint32_t>(j * gpj + lgrp) == win) taken |= 1u << j;
                     }
 #pragma unroll
                     for (int v = 0; v < V; ++v) {
-                        const int g = (v / 4) * gpj + lane / L;
+                        const int g = (v / 4) * gpj + lgrp;
                         if (!((kept >> g) & 1u)) key[v] = 0u;
                     }
                 } else {
