@@ -74,6 +74,8 @@ def _load():
             lib.orc_combine.restype = None
             lib.orc_combine_rows.argtypes = [P, P, P, P, i32, i32, i32, P]
             lib.orc_combine_rows.restype = None
+            lib.orc_plan_balanced.argtypes = [P, i32, i32, i32, i32, i32, ctypes.c_int32, i32, ctypes.c_int32] + [P] * 9
+            lib.orc_plan_balanced.restype = i32
             _lib = lib
     return _lib
 
@@ -226,4 +228,27 @@ def combine_rows(y_bits, w, dst, tokens):
     H = y.shape[1]
     out = np.empty((t.shape[0], H), np.uint16)
     _load().orc_combine_rows(_ptr(y), _ptr(wf), _ptr(d), _ptr(t), t.shape[0], K, H, _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------- balanced plan
+def plan_balanced(topk_idx, E, R, token_padding, capacity, B, NvS):
+    """Capacity-balanced plan with redundant experts (single source rank).
+
+    Returns dict(z[R,R], alloc[R,E], alloc_cumsum[E,R], experts_to_copy[R,B],
+    remote_stats[R,2], rank_cu_seqlens[R,E+B], rank_zero_fill[R,E+B,2],
+    expert_offsets[R,E], dst[N,K])."""
+    topk = _c(topk_idx, np.int32)
+    N, K = topk.shape
+    out = dict(z=np.empty((R, R), np.int32), alloc=np.empty((R, E), np.int32),
+               alloc_cumsum=np.empty((E, R), np.int32), experts_to_copy=np.empty((R, max(B, 0)), np.int32),
+               remote_stats=np.empty((R, 2), np.int32), rank_cu_seqlens=np.empty((R, E + B), np.int32),
+               rank_zero_fill=np.empty((R, E + B, 2), np.int32), expert_offsets=np.empty((R, E), np.int32),
+               dst=np.empty((N, K), np.int32))
+    rc = _load().orc_plan_balanced(
+        _ptr(topk), N, E, K, R, token_padding, int(capacity), B, int(NvS),
+        *[_ptr(out[k]) for k in ("z", "alloc", "alloc_cumsum", "experts_to_copy", "remote_stats",
+                                 "rank_cu_seqlens", "rank_zero_fill", "expert_offsets", "dst")])
+    if rc != OK:
+        raise OracleError(rc)
     return out

@@ -511,3 +511,245 @@ void orc_combine_rows(const uint16_t* y, const float* w, const int32_t* dst,
         }
     }
 }
+
+/* ------------------------------------------------------------------ */
+/* Capacity-balanced plan with redundant experts                       */
+/* ------------------------------------------------------------------ */
+/*
+ * MoonEP moonep/planning.py, PlanningKernel, the rank-0 planning steps and
+ * the dst computation, in their single-source form (one GPU holds every
+ * token, so the prefix over source ranks of tokens per expert is just the
+ * expert's count).  Steps, in the page's order:
+ *
+ *  S1  group_tokens[r] = pairs routed to rank r's experts.
+ *  Balance: balance[r] = group_tokens[r] - CAP.  While some rank has
+ *      balance > 0 and some < 0: surplus = the largest balance, deficit =
+ *      the smallest (ties: lower rank); move = -deficit tokens from the
+ *      surplus rank to the deficit rank: z[surplus][deficit] = move,
+ *      balance[surplus] -= move, balance[deficit] = 0.  Each step zeroes one
+ *      rank and a zeroed rank never moves again, so at most R steps.
+ *  Alloc (per owner rank o): quotas[r] = z[o][r]; remaining[le] = count of
+ *      o's le-th expert.  While the largest quota (ties: lower rank) and
+ *      the largest remaining count (ties: lower expert) are both positive:
+ *      take = min of the two; that many of the expert's pairs go to the
+ *      quota rank.  alloc[r][e] = pairs of expert e handled by rank r
+ *      (its owner keeps the rest); alloc_cumsum[e][r] = inclusive prefix
+ *      over r.
+ *  Selection (per destination rank d): remote[e] = alloc[d][e] for experts
+ *      not owned by d, else 0; remote_stats[d][0] = #{e : remote[e] > 0}.
+ *      B rounds: pick the largest remote count, ties to the HIGHER expert
+ *      index (the page's ">=" scan); experts_to_copy[d][slot] = that expert
+ *      if its count > 0, else -1; the pick is cleared; a real pick adds 1
+ *      to remote_stats[owner][1].
+ *  Groups g in [0, E+B) of rank d: g < E holds expert g with count
+ *      alloc[d][g] unless g was picked (then 0); g >= E holds the expert of
+ *      slot g-E with count alloc[d][that expert] (0 for -1).
+ *      padded = round_up(count, tp) if count > 0 else 0; base = exclusive
+ *      prefix of padded over g; cu_seqlens[d][g] = base + padded (padded
+ *      end, rank-local); zero_fill[d][g] = (base + count, padded - count)
+ *      when count > 0 and padded > count, else (0, 0); expert_offsets[d][e]
+ *      = base of the group holding expert e when its count > 0.  Reading:
+ *      entries the page leaves unwritten are 0.
+ *  dst: for pair f of expert e at position gr among e's pairs (ascending
+ *      flat index), the destination rank is the first r with
+ *      alloc_cumsum[e][r] > gr; pc = alloc_cumsum[e][r-1] (0 for r = 0);
+ *      dst[f] = r * NvS + expert_offsets[r][e] + (gr - pc).  Then the
+ *      duplicate canonicalisation by destination rank (dst / NvS), as in
+ *      the plain plan: a later pair of a token on an already-seen rank
+ *      stores -dst-1.
+ * Returns ORC_ECAP when a rank's groups need more than NvS rows.
+ */
+static int argmax_low_i32(const int32_t* v, int n) /* largest value, lowest index */
+{
+    int best = 0;
+    for (int i = 1; i < n; ++i)
+        if (v[i] > v[best])
+            best = i;
+    return best;
+}
+
+static int argmin_low_i32(const int32_t* v, int n) /* smallest value, lowest index */
+{
+    int best = 0;
+    for (int i = 1; i < n; ++i)
+        if (v[i] < v[best])
+            best = i;
+    return best;
+}
+
+int orc_plan_balanced(const int32_t* topk, int N, int E, int K, int R, int token_padding,
+                      int32_t capacity, int B, int32_t NvS,
+                      int32_t* z /* R*R */, int32_t* alloc /* R*E */, int32_t* alloc_cumsum /* E*R */,
+                      int32_t* experts_to_copy /* R*B */, int32_t* remote_stats /* R*2 */,
+                      int32_t* rank_cu_seqlens /* R*(E+B) */, int32_t* rank_zero_fill /* R*(E+B)*2 */,
+                      int32_t* expert_offsets /* R*E */, int32_t* dst /* N*K */)
+{
+    if (N < 1 || E < 1 || K < 1 || R < 1 || E % R != 0 || token_padding < 1 || B < 0 || NvS < 1)
+        return ORC_EINVAL;
+    const int epn = E / R;
+    const int64_t NK = (int64_t)N * K;
+    for (int64_t f = 0; f < NK; ++f)
+        if (topk[f] < 0 || topk[f] >= E)
+            return ORC_EINVAL;
+
+    int32_t* count = (int32_t*)calloc((size_t)E, sizeof(int32_t));
+    int32_t* pos = (int32_t*)malloc(sizeof(int32_t) * (size_t)(NK > 0 ? NK : 1));
+    int32_t* balance = (int32_t*)malloc(sizeof(int32_t) * (size_t)R);
+    int32_t* quotas = (int32_t*)malloc(sizeof(int32_t) * (size_t)R);
+    int32_t* remaining = (int32_t*)malloc(sizeof(int32_t) * (size_t)epn);
+    int32_t* remote = (int32_t*)malloc(sizeof(int32_t) * (size_t)E);
+    unsigned char* picked = (unsigned char*)malloc((size_t)E);
+    unsigned char* seen = (unsigned char*)malloc((size_t)R);
+    if (!count || !pos || !balance || !quotas || !remaining || !remote || !picked || !seen) {
+        free(count); free(pos); free(balance); free(quotas); free(remaining); free(remote);
+        free(picked); free(seen);
+        return ORC_ECAP;
+    }
+    int rc = ORC_OK;
+
+    /* histogram and stable positions */
+    for (int64_t f = 0; f < NK; ++f) {
+        pos[f] = count[topk[f]];
+        count[topk[f]] += 1;
+    }
+
+    /* S1 + balance */
+    for (int i = 0; i < R * R; ++i)
+        z[i] = 0;
+    for (int r = 0; r < R; ++r) {
+        int32_t g = 0;
+        for (int e = r * epn; e < (r + 1) * epn; ++e)
+            g += count[e];
+        balance[r] = g - capacity;
+    }
+    for (;;) {
+        int s = argmax_low_i32(balance, R);
+        int d = argmin_low_i32(balance, R);
+        if (balance[s] <= 0 || balance[d] >= 0)
+            break;
+        int32_t move = -balance[d];
+        balance[s] -= move;
+        balance[d] = 0;
+        z[s * R + d] = move;
+    }
+
+    /* alloc per owner rank */
+    for (int i = 0; i < R * E; ++i)
+        alloc[i] = 0;
+    for (int o = 0; o < R; ++o) {
+        for (int r = 0; r < R; ++r)
+            quotas[r] = z[o * R + r];
+        for (int le = 0; le < epn; ++le) {
+            remaining[le] = count[o * epn + le];
+            alloc[o * E + o * epn + le] = count[o * epn + le];
+        }
+        for (;;) {
+            int t = argmax_low_i32(quotas, R);
+            if (quotas[t] <= 0)
+                break;
+            int le = argmax_low_i32(remaining, epn);
+            if (remaining[le] <= 0)
+                break;
+            int32_t take = remaining[le] < quotas[t] ? remaining[le] : quotas[t];
+            quotas[t] -= take;
+            remaining[le] -= take;
+            alloc[t * E + o * epn + le] += take;
+            alloc[o * E + o * epn + le] = remaining[le];
+        }
+    }
+    for (int e = 0; e < E; ++e) {
+        int32_t cum = 0;
+        for (int r = 0; r < R; ++r) {
+            cum += alloc[r * E + e];
+            alloc_cumsum[e * R + r] = cum;
+        }
+    }
+
+    /* selection of redundant experts, per-rank groups */
+    for (int i = 0; i < R * 2; ++i)
+        remote_stats[i] = 0;
+    for (int i = 0; i < R * E; ++i)
+        expert_offsets[i] = 0;
+    for (int d = 0; d < R && rc == ORC_OK; ++d) {
+        int nremote = 0;
+        for (int e = 0; e < E; ++e) {
+            int local = e >= d * epn && e < (d + 1) * epn;
+            remote[e] = local ? 0 : alloc[d * E + e];
+            picked[e] = 0;
+            if (remote[e] > 0)
+                nremote += 1;
+        }
+        remote_stats[2 * d] = nremote;
+        for (int slot = 0; slot < B; ++slot) {
+            int best = 0;
+            for (int e = 1; e < E; ++e)
+                if (remote[e] >= remote[best])
+                    best = e; /* ties to the higher index */
+            int32_t cnt = remote[best];
+            remote[best] = 0;
+            int pick = cnt > 0 ? best : -1;
+            experts_to_copy[d * B + slot] = pick;
+            if (pick >= 0) {
+                remote_stats[2 * (pick / epn) + 1] += 1;
+                picked[pick] = 1;
+            }
+        }
+        int64_t base = 0;
+        for (int g = 0; g < E + B; ++g) {
+            int32_t c = 0;
+            int expert = -1;
+            if (g < E) {
+                if (!picked[g]) {
+                    c = alloc[d * E + g];
+                    expert = g;
+                }
+            } else {
+                int sel = experts_to_copy[d * B + (g - E)];
+                if (sel >= 0) {
+                    c = alloc[d * E + sel];
+                    expert = sel;
+                }
+            }
+            int64_t padded = c > 0 ? ((int64_t)c + token_padding - 1) / token_padding * token_padding : 0;
+            if (c > 0)
+                expert_offsets[d * E + expert] = (int32_t)base;
+            rank_cu_seqlens[d * (E + B) + g] = (int32_t)(base + padded);
+            if (c > 0 && padded > c) {
+                rank_zero_fill[2 * (d * (E + B) + g)] = (int32_t)(base + c);
+                rank_zero_fill[2 * (d * (E + B) + g) + 1] = (int32_t)(padded - c);
+            } else {
+                rank_zero_fill[2 * (d * (E + B) + g)] = 0;
+                rank_zero_fill[2 * (d * (E + B) + g) + 1] = 0;
+            }
+            base += padded;
+        }
+        if (base > NvS)
+            rc = ORC_ECAP;
+    }
+
+    /* dst by the prefix of allocations, then duplicates by rank */
+    for (int64_t f = 0; f < NK && rc == ORC_OK; ++f) {
+        int e = topk[f];
+        int32_t gr = pos[f];
+        int r = 0;
+        while (alloc_cumsum[e * R + r] <= gr)
+            r += 1;
+        int32_t pc = r > 0 ? alloc_cumsum[e * R + r - 1] : 0;
+        dst[f] = r * NvS + expert_offsets[r * E + e] + (gr - pc);
+    }
+    for (int s = 0; s < N && rc == ORC_OK; ++s) {
+        for (int r = 0; r < R; ++r)
+            seen[r] = 0;
+        for (int k = 0; k < K; ++k) {
+            int64_t f = (int64_t)s * K + k;
+            int r = dst[f] / NvS;
+            if (seen[r])
+                dst[f] = -dst[f] - 1;
+            seen[r] = 1;
+        }
+    }
+
+    free(count); free(pos); free(balance); free(quotas); free(remaining); free(remote);
+    free(picked); free(seen);
+    return rc;
+}
