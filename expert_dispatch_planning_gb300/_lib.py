@@ -16,6 +16,7 @@ MOE_ERR_CUDA = 4
 MOE_ERR_DEVICE_TIMEOUT = 5
 MOE_ERR_DEVICE_INDEX = 6
 MOE_ERR_WORKSPACE = 7
+MOE_ERR_DEVICE_CAPACITY = 8
 
 MOE_SCORING_SOFTMAX = 0
 MOE_SCORING_SIGMOID = 1
@@ -34,6 +35,12 @@ class MoePlanOut(ctypes.Structure):
         "dup_loffs", "dup_counts", "status")]
 
 
+class MoeBalancedPlanOut(ctypes.Structure):
+    _fields_ = [(name, _P) for name in (
+        "z", "alloc", "alloc_cumsum", "experts_to_copy", "remote_stats", "rank_cu_seqlens", "rank_zero_fill",
+        "expert_offsets", "dst")]
+
+
 # (name, restype, argtypes) for every function include/moe_dispatch.h declares
 SIGNATURES = [
     ("moe_status_string", ctypes.c_char_p, [_i32]),
@@ -44,6 +51,8 @@ SIGNATURES = [
     ("moe_plan_workspace_init", _i32, [_P, _size, _P]),
     ("moe_plan", _i32, [_P, _i32, _i32, _i32, _i32, _i32, _P, _size, ctypes.POINTER(MoePlanOut), _P]),
     ("moe_plan_no_alloc", _i32, [_P, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(MoePlanOut), _P]),
+    ("moe_plan_balanced", _i32, [ctypes.POINTER(MoePlanOut), _P, _i32, _i32, _i32, _i32, _i32, ctypes.c_int32,
+                                 _i32, ctypes.c_int32, ctypes.POINTER(MoeBalancedPlanOut), _P]),
     ("moe_permute", _i32, [_P, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(MoePlanOut), _P, _P]),
     ("moe_combine", _i32, [_P, _P, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(MoePlanOut), _P, _P]),
     ("moe_get_status", _i32, [ctypes.POINTER(MoePlanOut), ctypes.POINTER(ctypes.c_int32), _P]),

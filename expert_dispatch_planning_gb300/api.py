@@ -11,7 +11,7 @@ from dataclasses import dataclass, field
 import torch
 
 from . import _lib
-from ._lib import MoePlanOut, check, load
+from ._lib import MoeBalancedPlanOut, MoePlanOut, check, load
 
 SCORING = {"softmax": _lib.MOE_SCORING_SOFTMAX, "sigmoid": _lib.MOE_SCORING_SIGMOID,
            0: 0, 1: 1}
@@ -144,6 +144,58 @@ def plan_launches(N: int, E: int, K: int, R: int) -> int:
     if n < 0:
         raise ValueError("unsupported plan sizes")
     return n
+
+
+@dataclass
+class BalancedPlan:
+    """Caller-owned outputs of the capacity-balanced plan (device tensors)."""
+    N: int
+    E: int
+    K: int
+    R: int
+    B: int
+    z: torch.Tensor
+    alloc: torch.Tensor
+    alloc_cumsum: torch.Tensor
+    experts_to_copy: torch.Tensor
+    remote_stats: torch.Tensor
+    rank_cu_seqlens: torch.Tensor
+    rank_zero_fill: torch.Tensor
+    expert_offsets: torch.Tensor
+    dst: torch.Tensor
+    c_struct: MoeBalancedPlanOut = field(default=None, repr=False)
+
+    FIELDS = ("z", "alloc", "alloc_cumsum", "experts_to_copy", "remote_stats", "rank_cu_seqlens",
+              "rank_zero_fill", "expert_offsets", "dst")
+
+    @classmethod
+    def allocate(cls, N, E, K, R, B, device="cuda") -> "BalancedPlan":
+        i32 = dict(dtype=torch.int32, device=device)
+        b = cls(N=N, E=E, K=K, R=R, B=B, z=torch.empty((R, R), **i32), alloc=torch.empty((R, E), **i32),
+                alloc_cumsum=torch.empty((E, R), **i32), experts_to_copy=torch.empty((R, max(B, 1)), **i32),
+                remote_stats=torch.empty((R, 2), **i32), rank_cu_seqlens=torch.empty((R, E + B), **i32),
+                rank_zero_fill=torch.empty((R, E + B, 2), **i32), expert_offsets=torch.empty((R, E), **i32),
+                dst=torch.empty((N, K), **i32))
+        b.c_struct = MoeBalancedPlanOut(*[getattr(b, k).data_ptr() for k in cls.FIELDS])
+        return b
+
+    def to_host(self) -> dict:
+        out = {k: getattr(self, k).cpu().numpy() for k in self.FIELDS}
+        out["experts_to_copy"] = out["experts_to_copy"][:, : self.B]
+        return out
+
+
+def plan_balanced(topk_idx: torch.Tensor, p: Plan, token_padding: int, capacity: int, B: int, NvS: int,
+                  out: BalancedPlan | None = None, stream=None) -> BalancedPlan:
+    """Capacity-balanced plan with redundant experts on top of the plain plan `p`."""
+    N, K = topk_idx.shape
+    _need(topk_idx, torch.int32, (p.N, p.K), "topk_idx")
+    if out is None:
+        out = BalancedPlan.allocate(N, p.E, K, p.R, B, device=topk_idx.device)
+    rc = load().moe_plan_balanced(ctypes.byref(p.c_struct), _ptr(topk_idx), N, p.E, K, p.R, int(token_padding),
+                                  int(capacity), int(B), int(NvS), ctypes.byref(out.c_struct), _stream(stream))
+    check("moe_plan_balanced", rc)
+    return out
 
 
 def permute(x: torch.Tensor, p: Plan, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:

@@ -51,6 +51,7 @@ extern "C" MOE_API const char* moe_status_string(int code) {
         case MOE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
         case MOE_ERR_DEVICE_INDEX: return "device index out of range";
         case MOE_ERR_WORKSPACE: return "plan workspace not initialised";
+        case MOE_ERR_DEVICE_CAPACITY: return "rank row budget exceeded";
         default: return "unknown status";
     }
 }

@@ -78,6 +78,14 @@ __device__ __forceinline__ int rank_of(const PlanArgs& a, int e) {
     return static_cast<int>((static_cast<uint64_t>(static_cast<uint32_t>(e)) * a.epn_magic) >> 32);
 }
 
+// First 16-byte boundary at or after p, measured from the start of the
+// dynamic shared memory block (the tile's is_token_in_rank bytes are copied
+// out with 16-byte vectors).
+__device__ __forceinline__ uint8_t* align16_after(int32_t* base, int32_t* p) {
+    const ptrdiff_t ints = p - base;
+    return reinterpret_cast<uint8_t*>(base + ((ints + 3) & ~static_cast<ptrdiff_t>(3)));
+}
+
 __device__ __forceinline__ uint64_t pack_flag(uint32_t epoch, uint32_t st, uint32_t v) {
     return (static_cast<uint64_t>(flag_tag(epoch)) << 32) | (static_cast<uint64_t>(st) << 30) | (v & 0x3fffffffu);
 }
@@ -528,7 +536,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_scatter_kernel(const PlanAr
     uint2* s_items = reinterpret_cast<uint2*>(s_dyn);                  // [PLAN_WARPS][ipt][32]
     int32_t* s_wc = s_dyn + 2 * PLAN_WARPS * 32 * a.ipt;               // [PLAN_WARPS][E]
     int32_t* s_base = s_wc + PLAN_WARPS * a.E;                         // [E]
-    uint8_t* s_itr = reinterpret_cast<uint8_t*>(s_base + a.E);         // [tile_tokens][R]
+    uint8_t* s_itr = align16_after(s_dyn, s_base + a.E);               // [tile_tokens][R]
     __shared__ int32_t s_wg[PLAN_WARPS], s_wd[PLAN_WARPS];
     __shared__ int32_t s_bad;
 
@@ -600,7 +608,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_cluster_kernel(const PlanAr
     int32_t* s_base = s_tot + C;                  // [E]
     int32_t* s_pad = s_base + E;                  // [E + R + 2]
     int32_t* s_cu = s_pad + E + R + 2;            // [E + R + 2]
-    uint8_t* s_itr = reinterpret_cast<uint8_t*>(s_cu + E + R + 2);  // [tile_tokens][R]
+    uint8_t* s_itr = align16_after(s_dyn, s_cu + E + R + 2);  // [tile_tokens][R]
     __shared__ int32_t s_wg[PLAN_WARPS], s_wd[PLAN_WARPS], s_warp[PLAN_WARPS + 1];
     __shared__ int32_t s_gd[2];
 
@@ -741,7 +749,7 @@ bool cluster_geometry(int N, int E, int K, int R, Geom* g) {
 
 size_t cluster_smem(const Geom& g, int E, int R) {
     const size_t ints = static_cast<size_t>(2 * moe::PLAN_WARPS * 32) * g.ipt + static_cast<size_t>(moe::PLAN_WARPS) * E +
-                        2 * static_cast<size_t>(g.C) + E + 2 * static_cast<size_t>(E + R + 2);
+                        2 * static_cast<size_t>(g.C) + E + 2 * static_cast<size_t>(E + R + 2) + 4;  // + alignment
     return sizeof(int32_t) * ints + (static_cast<size_t>(g.tile_tokens) * R + 15) / 16 * 16;
 }
 
@@ -890,7 +898,7 @@ extern "C" MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, in
     // ---- two launches: decoupled look-back over tiles, then the scatter
     const size_t smem1 = sizeof(int32_t) * (static_cast<size_t>(g.C) + 2 * (E + R + 2) + 2);
     const size_t smem2 = sizeof(int32_t) * (static_cast<size_t>(moe::PLAN_WARPS + 1) * E +
-                                            static_cast<size_t>(2 * moe::PLAN_WARPS * 32) * g.ipt) +
+                                            static_cast<size_t>(2 * moe::PLAN_WARPS * 32) * g.ipt + 4) +
                          (static_cast<size_t>(g.tile_tokens) * R + 15) / 16 * 16;
     rc = moe_host::launch(moe::plan_count_kernel, dim3(g.T), dim3(moe::PLAN_THREADS), smem1, stream, a);
     if (rc != MOE_OK) return rc;

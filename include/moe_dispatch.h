@@ -59,6 +59,7 @@ extern "C" {
 #define MOE_ERR_DEVICE_TIMEOUT 5   /* (device) a bounded wait ran out                */
 #define MOE_ERR_DEVICE_INDEX 6     /* (device) an expert id or slot out of range     */
 #define MOE_ERR_WORKSPACE 7        /* (device) plan workspace not initialised        */
+#define MOE_ERR_DEVICE_CAPACITY 8  /* (device) a rank's groups exceed its row budget */
 
 #define MOE_SCORING_SOFTMAX 0
 #define MOE_SCORING_SIGMOID 1
@@ -206,6 +207,46 @@ MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, int R, int al
  */
 MOE_API int moe_plan_no_alloc(const int32_t* topk_idx, int N, int E, int K, int R, int alignment,
                               const MoePlanOut* out, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- balanced plan */
+/*
+ * Capacity-balanced logical-rank plan with redundant experts (MoonEP
+ * moonep/planning.py, PlanningKernel: the balancing matrix z, the
+ * allocation of each owner's expert pairs to other ranks, the top-B remote
+ * expert selection, per-rank padded groups, and dst by the allocation
+ * prefix in the rank*NvS + loff encoding), in its one-GPU form: a single
+ * source rank, so the per-expert token totals are the plain plan's counts.
+ * All arrays are caller-owned device memory, int32, 4-byte aligned.
+ */
+typedef struct MoeBalancedPlanOut {
+    int32_t* z;                /* [R][R]  pairs moved from rank i to rank j              */
+    int32_t* alloc;            /* [R][E]  pairs of expert e handled by rank r            */
+    int32_t* alloc_cumsum;     /* [E][R]  inclusive prefix of alloc over ranks           */
+    int32_t* experts_to_copy;  /* [R][B]  redundant experts per rank, -1 for none        */
+    int32_t* remote_stats;     /* [R][2]  (remote experts with pairs, times picked)      */
+    int32_t* rank_cu_seqlens;  /* [R][E+B] padded group ends, rank-local                 */
+    int32_t* rank_zero_fill;   /* [R][E+B][2] (start, count) of each group's padding     */
+    int32_t* expert_offsets;   /* [R][E]  first row of expert e's group on rank r (0 if
+                                  the rank holds none of its pairs)                      */
+    int32_t* dst;              /* [N][K]  r*NvS + row on rank r; -value-1 for a later
+                                  pair of the token on an already-used rank              */
+} MoeBalancedPlanOut;
+
+/*
+ * plan         a plan built by moe_plan for the same topk_idx (its counts,
+ *              cu_seqlens and dst give each pair's position among its
+ *              expert's pairs); its status word receives device errors.
+ * capacity     CAP: pairs a rank should hold before balancing moves pairs to
+ *              ranks below it (MoonEP's NvS_capacity).
+ * B            redundant-expert slots per rank, 0 <= B <= 64.
+ * token_padding  rows each group is padded to (>= 1).
+ * NvS          rows per rank in the dst encoding; R*NvS < 2^31.  A rank whose
+ *              groups need more rows sets MOE_ERR_DEVICE_CAPACITY.
+ * Two launches on `stream` after the plain plan; no workspace.
+ */
+MOE_API int moe_plan_balanced(const MoePlanOut* plan, const int32_t* topk_idx, int N, int E, int K, int R,
+                              int token_padding, int32_t capacity, int B, int32_t NvS,
+                              const MoeBalancedPlanOut* out, cudaStream_t stream);
 
 /* ---------------------------------------------------------------- rows */
 /*

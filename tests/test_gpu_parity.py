@@ -143,7 +143,11 @@ def test_plan_configs(m, name, plan_path):
     (333, 16, 1, 1, 4, "rand"), (1000, 8, 8, 8, 3, "rand"), (4097, 64, 3, 16, 16, "rand"),
     (5000, 32, 6, 32, 7, "rand"), (2500, 128, 16, 8, 64, "rand"), (700, 64, 32, 2, 2, "rand"),
     (9000, 8, 2, 4, 16, "hot"), (3000, 1024, 8, 128, 128, "rand"), (2049, 24, 5, 3, 9, "dups"),
-    (600, 16, 4, 4, 5, "one"), (12345, 256, 8, 64, 128, "rand"), (20000, 96, 1, 96, 32, "rand")])
+    (600, 16, 4, 4, 5, "one"), (12345, 256, 8, 64, 128, "rand"), (20000, 96, 1, 96, 32, "rand"),
+    # small and odd E / R: the shared-memory staging of is_token_in_rank must
+    # stay 16-byte aligned for every layout
+    (1134, 2, 1, 2, 1, "rand"), (777, 6, 2, 3, 5, "rand"), (333, 3, 3, 1, 2, "rand"),
+    (2000, 10, 3, 5, 7, "rand"), (9001, 2, 2, 1, 4, "rand"), (40000, 6, 1, 2, 3, "rand")])
 def test_plan_shapes(m, N, E, K, R, a, mode, plan_path):
     rng = np.random.default_rng(N + E + K)
     if mode == "one":      # every pair on expert 3: empty experts, one full
