@@ -76,6 +76,10 @@ def _load():
             lib.orc_combine_rows.restype = None
             lib.orc_plan_balanced.argtypes = [P, i32, i32, i32, i32, i32, ctypes.c_int32, i32, ctypes.c_int32] + [P] * 9
             lib.orc_plan_balanced.restype = i32
+            lib.orc_tile_map.argtypes = [P, i32, i32, P, P, i64, P]
+            lib.orc_tile_map.restype = i32
+            lib.orc_rank_layout.argtypes = [P, i32, i32, i32, P, P]
+            lib.orc_rank_layout.restype = i32
             _lib = lib
     return _lib
 
@@ -252,3 +256,28 @@ def plan_balanced(topk_idx, E, R, token_padding, capacity, B, NvS):
     if rc != OK:
         raise OracleError(rc)
     return out
+
+
+# ---------------------------------------------------------------- tile map / rank layout
+def tile_map(tokens_per_expert, tile, max_tiles):
+    """Grouped-GEMM tiles: (tile_expert[max_tiles], tile_row_limit[max_tiles], (num_tiles, size))."""
+    c = _c(tokens_per_expert, np.int32)
+    te = np.empty(max_tiles, np.int32)
+    tl = np.empty(max_tiles, np.int32)
+    sizes = np.empty(2, np.int32)
+    rc = _load().orc_tile_map(_ptr(c), c.size, int(tile), _ptr(te), _ptr(tl), int(max_tiles), _ptr(sizes))
+    if rc != OK:
+        raise OracleError(rc)
+    return te, tl, sizes
+
+
+def rank_layout(is_token_in_rank, num_channels):
+    """(channel_prefix_matrix[R, C], token_rank_slot[N, R]) from is_token_in_rank[N, R]."""
+    itr = _c(is_token_in_rank, np.uint8)
+    N, R = itr.shape
+    cpm = np.empty((R, num_channels), np.int32)
+    trs = np.empty((N, R), np.int32)
+    rc = _load().orc_rank_layout(_ptr(itr), N, R, int(num_channels), _ptr(cpm), _ptr(trs))
+    if rc != OK:
+        raise OracleError(rc)
+    return cpm, trs

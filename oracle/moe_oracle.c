@@ -753,3 +753,93 @@ int orc_plan_balanced(const int32_t* topk, int N, int E, int K, int R, int token
     free(picked); free(seen);
     return rc;
 }
+
+/* ------------------------------------------------------------------ */
+/* Grouped-GEMM tile map                                               */
+/* ------------------------------------------------------------------ */
+/*
+ * TensorRT-LLM RoutingKernel.cuh, routingPermutation: for each expert
+ * numCta = ceil(count / tile) tiles of `tile` rows; ctaOffset = exclusive
+ * prefix of numCta over experts; tile ctaOffset + j (j < numCta) belongs to
+ * the expert (CtaIdxXyToBatchIdx) and ends at row
+ * min((ctaOffset + j + 1) * tile, ctaOffset * tile + count)
+ * (CtaIdxXyToMnLimit); NumNonExitingCtas = sum numCta; PermutedIdxSize =
+ * NumNonExitingCtas * tile.  Reading: global expert ids over all experts
+ * (the page filters a rank's local experts), and tiles from num_tiles up to
+ * max_tiles hold -1.
+ */
+int orc_tile_map(const int32_t* counts, int E, int tile, int32_t* tile_expert, int32_t* tile_row_limit,
+                 int64_t max_tiles, int32_t* sizes)
+{
+    if (E < 1 || tile < 1)
+        return ORC_EINVAL;
+    int64_t cta_offset = 0;
+    for (int e = 0; e < E; ++e) {
+        if (counts[e] < 0)
+            return ORC_EINVAL;
+        int64_t num_cta = ((int64_t)counts[e] + tile - 1) / tile;
+        for (int64_t j = 0; j < num_cta; ++j) {
+            int64_t t = cta_offset + j;
+            if (t >= max_tiles)
+                return ORC_ECAP;
+            int64_t lim1 = (cta_offset + j + 1) * tile;
+            int64_t lim2 = cta_offset * tile + counts[e];
+            tile_expert[t] = e;
+            tile_row_limit[t] = (int32_t)(lim1 < lim2 ? lim1 : lim2);
+        }
+        cta_offset += num_cta;
+    }
+    for (int64_t t = cta_offset; t < max_tiles; ++t) {
+        tile_expert[t] = -1;
+        tile_row_limit[t] = -1;
+    }
+    sizes[0] = (int32_t)cta_offset;
+    sizes[1] = (int32_t)(cta_offset * tile);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* Rank layout: channel prefix matrix, deduplicated per-rank slots      */
+/* ------------------------------------------------------------------ */
+/*
+ * DeepEP csrc/kernels/intranode.cu, notify_dispatch: for each destination
+ * rank and channel, the number of the channel's tokens that go to the rank
+ * (is_token_in_rank), then an inclusive prefix over channels
+ * (channel_prefix_matrix[r][c]).  Reading: channel c covers tokens
+ * [min(c*q, N), min((c+1)*q, N)) with q = ceil(N / C) (the helper that
+ * splits tokens is not on the page).
+ * token_rank_slot[s][r]: reading of DeepEP's per-(token, rank) send slot
+ * with one source rank: a token goes to each rank it needs exactly once,
+ * ranks' blocks follow each other (rank_prefix = exclusive prefix of
+ * tokens per rank) and tokens keep their order inside a block:
+ * rank_prefix[r] + #{s' < s : is_token_in_rank[s'][r]}, or -1.
+ */
+int orc_rank_layout(const uint8_t* is_token_in_rank, int N, int R, int C, int32_t* channel_prefix_matrix,
+                    int32_t* token_rank_slot)
+{
+    if (N < 1 || R < 1 || C < 1)
+        return ORC_EINVAL;
+    int64_t q = ((int64_t)N + C - 1) / C;
+    int32_t base = 0;
+    for (int r = 0; r < R; ++r) {
+        int32_t run = 0;
+        for (int c = 0; c < C; ++c) {
+            int64_t b = (int64_t)c * q < N ? (int64_t)c * q : N;
+            int64_t e = ((int64_t)c + 1) * q < N ? ((int64_t)c + 1) * q : N;
+            for (int64_t s = b; s < e; ++s)
+                run += is_token_in_rank[s * R + r] ? 1 : 0;
+            channel_prefix_matrix[r * C + c] = run;
+        }
+        int32_t pos = 0;
+        for (int64_t s = 0; s < N; ++s) {
+            if (is_token_in_rank[s * R + r]) {
+                token_rank_slot[s * R + r] = base + pos;
+                pos += 1;
+            } else {
+                token_rank_slot[s * R + r] = -1;
+            }
+        }
+        base += pos;
+    }
+    return ORC_OK;
+}
