@@ -53,6 +53,8 @@ SIGNATURES = [
     ("moe_plan_no_alloc", _i32, [_P, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(MoePlanOut), _P]),
     ("moe_plan_balanced", _i32, [ctypes.POINTER(MoePlanOut), _P, _i32, _i32, _i32, _i32, _i32, ctypes.c_int32,
                                  _i32, ctypes.c_int32, ctypes.POINTER(MoeBalancedPlanOut), _P]),
+    ("moe_tile_map", _i32, [ctypes.POINTER(MoePlanOut), _i32, _i32, _P, _P, _i64, _P, _P]),
+    ("moe_rank_layout", _i32, [ctypes.POINTER(MoePlanOut), _i32, _i32, _i32, _P, _P, _P]),
     ("moe_permute", _i32, [_P, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(MoePlanOut), _P, _P]),
     ("moe_combine", _i32, [_P, _P, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(MoePlanOut), _P, _P]),
     ("moe_get_status", _i32, [ctypes.POINTER(MoePlanOut), ctypes.POINTER(ctypes.c_int32), _P]),

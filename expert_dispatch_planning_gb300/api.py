@@ -198,6 +198,29 @@ def plan_balanced(topk_idx: torch.Tensor, p: Plan, token_padding: int, capacity:
     return out
 
 
+def tile_map(p: Plan, max_tiles: int | None = None, stream=None):
+    """Grouped-GEMM tiles of `p.alignment` rows: (tile_expert, tile_row_limit, sizes[num_tiles, P])."""
+    if max_tiles is None:
+        max_tiles = max(1, p.P_cap // p.alignment)
+    dev = p.dst.device
+    te = torch.empty(max_tiles, dtype=torch.int32, device=dev)
+    tl = torch.empty(max_tiles, dtype=torch.int32, device=dev)
+    sizes = torch.empty(2, dtype=torch.int32, device=dev)
+    check("moe_tile_map", load().moe_tile_map(ctypes.byref(p.c_struct), p.E, p.alignment, _ptr(te), _ptr(tl),
+                                             int(max_tiles), _ptr(sizes), _stream(stream)))
+    return te, tl, sizes
+
+
+def rank_layout(p: Plan, num_channels: int, stream=None):
+    """(channel_prefix_matrix[R, C], token_rank_slot[N, R]) of a plan."""
+    dev = p.dst.device
+    cpm = torch.empty((p.R, num_channels), dtype=torch.int32, device=dev)
+    trs = torch.empty((p.N, p.R), dtype=torch.int32, device=dev)
+    check("moe_rank_layout", load().moe_rank_layout(ctypes.byref(p.c_struct), p.N, p.R, int(num_channels),
+                                                   _ptr(cpm), _ptr(trs), _stream(stream)))
+    return cpm, trs
+
+
 def permute(x: torch.Tensor, p: Plan, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Expert-contiguous copy of x bf16[N,H] -> bf16[P_cap,H] (rows >= P untouched)."""
     N, H = x.shape

@@ -248,6 +248,36 @@ MOE_API int moe_plan_balanced(const MoePlanOut* plan, const int32_t* topk_idx, i
                               int token_padding, int32_t capacity, int B, int32_t NvS,
                               const MoeBalancedPlanOut* out, cudaStream_t stream);
 
+/* ---------------------------------------------------------------- layouts */
+/*
+ * Grouped-GEMM tile map (TensorRT-LLM RoutingKernel.cuh, routingPermutation:
+ * CtaIdxXyToBatchIdx, CtaIdxXyToMnLimit, NumNonExitingCtas,
+ * PermutedIdxSize) over a plan's permuted buffer, with tiles of `alignment`
+ * rows (the plan's alignment, so every expert starts on a tile).
+ *   tile_expert     (device) int32[max_tiles]: expert of tile t (global id),
+ *                   -1 from num_tiles on.
+ *   tile_row_limit  (device) int32[max_tiles]: one past the tile's last real
+ *                   row, min((t+1)*alignment, cu[e] + count[e]); -1 past the end.
+ *   sizes           (device) int32[2]: (num_tiles, padded rows P).
+ * max_tiles >= P_cap / alignment covers every plan of these sizes.
+ */
+MOE_API int moe_tile_map(const MoePlanOut* plan, int E, int alignment, int32_t* tile_expert,
+                         int32_t* tile_row_limit, int64_t max_tiles, int32_t* sizes, cudaStream_t stream);
+
+/*
+ * Rank layout (DeepEP csrc/kernels/intranode.cu, notify_dispatch).
+ *   channel_prefix_matrix  (device) int32[R][num_channels]: tokens of channels
+ *                   0..c that go to rank r; channel c covers tokens
+ *                   [c*q, (c+1)*q), q = ceil(N / num_channels).
+ *   token_rank_slot (device) int32[N][R]: the row of token s in a buffer that
+ *                   holds each token once per rank it needs, ranks' blocks
+ *                   at rank_prefix[r], tokens in order; -1 if s does not go
+ *                   to r.
+ * Reads the plan's is_token_in_rank and rank_prefix.  R <= 128.
+ */
+MOE_API int moe_rank_layout(const MoePlanOut* plan, int N, int R, int num_channels,
+                            int32_t* channel_prefix_matrix, int32_t* token_rank_slot, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- rows */
 /*
  * Permute (DeepEP dispatch's hidden-row copy, MoonEP dst / zero_fill_ranges):
