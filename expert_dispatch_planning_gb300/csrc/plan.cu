@@ -40,7 +40,7 @@
 
 namespace moe {
 
-constexpr int PLAN_THREADS = 512;
+constexpr int PLAN_THREADS = 1024;
 constexpr int PLAN_WARPS = PLAN_THREADS / 32;
 constexpr int PLAN_IPT_MAX = 8;
 constexpr int LOOKBACK_WINDOW = 16;
@@ -260,9 +260,12 @@ __device__ __noinline__ void tile_phase1(const PlanArgs& a, int tile, int32_t* s
         const int groups_before = __shfl_sync(FULL_MASK, excl, my_p) - tok_base;
         const int before = groups_before + (dup ? __popc(pd & lt) - 1 : 0);
         const int dup_pos = run_d + __popc(dball & below_tok) + before;
-        if (prim) {
-            s_itr[(s - tok0) * R + r] = 1;
-            if (s_rtok != nullptr) atomicAdd(&s_rtok[r], 1);
+        if (prim) s_itr[(s - tok0) * R + r] = 1;
+        if (s_rtok != nullptr) {
+            // tokens per rank: one add per distinct rank of the warp step
+            // (per-lane adds on R counters serialise)
+            const unsigned pr = __match_any_sync(FULL_MASK, prim ? r : -1);
+            if (prim && (pr & lt) == 0u) atomicAdd(&s_rtok[r], __popc(pr));
         }
         s_items[(warp * a.ipt + i) * 32 + lane] =
             active ? pack_item(e, wr, dup, opens, __popc(pd) - 1, opens ? run_g + __popc(gball & lt) : dup_pos, dup_pos)
@@ -276,9 +279,9 @@ __device__ __noinline__ void tile_phase1(const PlanArgs& a, int tile, int32_t* s
     }
 }
 
-// Exclusive scan of 16 per-warp values by one warp (lane w holds warp w's
-// value); returns the base of lane's warp and writes it back.
-__device__ __forceinline__ void warp_scan16(int32_t* s_val, int32_t base) {
+// Exclusive scan of the per-warp-run values by one warp (lane w holds warp
+// run w's value), written back with `base` added.
+__device__ __forceinline__ void warp_scan_runs(int32_t* s_val, int32_t base) {
     const int lane = threadIdx.x & 31;
     int32_t v = lane < PLAN_WARPS ? s_val[lane] : 0;
     int32_t incl = v;
@@ -300,17 +303,22 @@ __device__ __noinline__ void tile_phase3(const PlanArgs& a, int tile, const int3
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int E = a.E, K = a.K, R = a.R;
     const int64_t tok0 = static_cast<int64_t>(tile) * a.tile_tokens;
+    // per (warp run, expert): the expert's pairs in earlier warp runs; a
+    // thread per expert (neighbouring threads, neighbouring banks), all its
+    // loads issued before the running sum
     for (int e = tid; e < E; e += PLAN_THREADS) {
+        int32_t v[PLAN_WARPS];
+#pragma unroll
+        for (int w = 0; w < PLAN_WARPS; ++w) v[w] = s_wc[w * E + e];
         int32_t run = s_base[e];
 #pragma unroll
         for (int w = 0; w < PLAN_WARPS; ++w) {
-            const int32_t v = s_wc[w * E + e];
             s_wc[w * E + e] = run;
-            run += v;
+            run += v[w];
         }
     }
-    if (warp == PLAN_WARPS - 1) warp_scan16(s_wg, g_base);
-    if (warp == PLAN_WARPS - 2) warp_scan16(s_wd, d_base);
+    if (warp == PLAN_WARPS - 1) warp_scan_runs(s_wg, g_base);
+    if (warp == PLAN_WARPS - 2) warp_scan_runs(s_wd, d_base);
     __syncthreads();
 
     const int tok_in_iter = lane / K, k = lane - (lane / K) * K;
@@ -371,16 +379,20 @@ __device__ __noinline__ void tile_phase3(const PlanArgs& a, int tile, const int3
 // the unused rows [P, P_cap).
 __device__ __forceinline__ void fill_unused(const PlanArgs& a, int tile, int T, const int32_t* cu, const int32_t* cnt) {
     const int tid = threadIdx.x;
-    for (int e = tile; e < a.E; e += T) {
-        const int32_t start = cu[e] + cnt[e];
-        const int32_t n = cu[e + 1] - start;
-        for (int j = tid; j < n; j += PLAN_THREADS)
-            if (start >= 0 && static_cast<int64_t>(start) + j < a.p_cap) a.out.src_of_slot[start + j] = -1;
+    const int per = a.alignment - 1;  // at most this many padding rows per expert
+    if (per > 0) {
+        const int mine = (a.E - tile + T - 1) / T;  // experts tile, tile + T, ...
+        for (int i = tid; i < mine * per; i += PLAN_THREADS) {
+            const int e = tile + (i / per) * T, j = i - (i / per) * per;
+            const int32_t start = cu[e] + cnt[e];
+            if (j < cu[e + 1] - start && start >= 0 && static_cast<int64_t>(start) + j < a.p_cap)
+                a.out.src_of_slot[start + j] = -1;
+        }
     }
     const int64_t P = cu[a.E];
     const int64_t rest = a.p_cap - P;
-    const int64_t per = (rest + T - 1) / T;
-    const int64_t b = P + per * tile, e = min(a.p_cap, b + per);
+    const int64_t share = (rest + T - 1) / T;
+    const int64_t b = P + share * tile, e = min(a.p_cap, b + share);
     for (int64_t j = b + tid; j < e; j += PLAN_THREADS) a.out.src_of_slot[j] = -1;
 }
 
@@ -437,11 +449,10 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_count_kernel(const PlanArgs
             const unsigned key = active ? static_cast<unsigned>(tok_in_iter * 128 + r) : 0xffffffffu;
             const unsigned pd = __match_any_sync(FULL_MASK, key);
             const bool prim = active && (pd & lt) == 0u;
-            if (prim) {
-                atomicAdd(&s_tot[E + r], 1);
-                if (__popc(pd) >= 2) ++my_groups;
-            }
+            if (prim && __popc(pd) >= 2) ++my_groups;
             if (active && !prim) ++my_dups;
+            const unsigned pr = __match_any_sync(FULL_MASK, prim ? r : -1);
+            if (prim && (pr & lt) == 0u) atomicAdd(&s_tot[E + r], __popc(pr));
         }
         my_groups = __reduce_add_sync(FULL_MASK, my_groups);
         my_dups = __reduce_add_sync(FULL_MASK, my_dups);
@@ -632,14 +643,14 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_cluster_kernel(const PlanAr
         for (int w = 0; w < PLAN_WARPS; ++w) c += s_wc[w * E + e];
         s_cnt[e] = c;
     }
-    if (tid == 0) {
-        int32_t g = 0, d = 0;
-        for (int w = 0; w < PLAN_WARPS; ++w) {
-            g += s_wg[w];
-            d += s_wd[w];
+    if ((tid >> 5) == 0) {
+        const int lane = tid & 31;
+        const int32_t g = __reduce_add_sync(FULL_MASK, lane < PLAN_WARPS ? s_wg[lane] : 0);
+        const int32_t d = __reduce_add_sync(FULL_MASK, lane < PLAN_WARPS ? s_wd[lane] : 0);
+        if (lane == 0) {
+            s_cnt[E + R] = g;
+            s_cnt[E + R + 1] = d;
         }
-        s_cnt[E + R] = g;
-        s_cnt[E + R + 1] = d;
     }
     cluster_arrive();  // counts of every tile visible cluster-wide
     cluster_wait();
@@ -699,7 +710,20 @@ Geom plan_geometry(int N, int E, int K, int R) {
     if (forced > 0) ipt = forced;
     if (ipt < 1) ipt = 1;
     if (ipt > moe::PLAN_IPT_MAX) ipt = moe::PLAN_IPT_MAX;
-    while (ipt > 1 && static_cast<int64_t>(moe::PLAN_WARPS) * ipt * g.tpw * R > 65536) --ipt;
+    // shared memory of the scatter kernel: per-pair items, per-warp expert
+    // counts, the tile's is_token_in_rank rows; shrink steps, then tokens per
+    // step, until it fits and the rows stay within 64 KB
+    auto smem2 = [&](int64_t st, int64_t tpw) {
+        return 4 * (2 * moe::PLAN_WARPS * 32 * st + static_cast<int64_t>(moe::PLAN_WARPS + 1) * E + 4) +
+               (moe::PLAN_WARPS * st * tpw * R + 15) / 16 * 16;
+    };
+    constexpr int64_t kSmemBudget = 220 * 1024;
+    while (ipt > 1 && (static_cast<int64_t>(moe::PLAN_WARPS) * ipt * g.tpw * R > 65536 ||
+                       smem2(ipt, g.tpw) > kSmemBudget))
+        --ipt;
+    while (g.tpw > 1 && (static_cast<int64_t>(moe::PLAN_WARPS) * ipt * g.tpw * R > 65536 ||
+                         smem2(ipt, g.tpw) > kSmemBudget))
+        g.tpw >>= 1;
     g.ipt = static_cast<int>(ipt);
     g.tile_tokens = moe::PLAN_WARPS * g.ipt * g.tpw;
     g.T = static_cast<int>((static_cast<int64_t>(N) + g.tile_tokens - 1) / g.tile_tokens);
@@ -729,6 +753,8 @@ namespace {
 
 constexpr int kMaxClusterTiles = 16;
 
+size_t cluster_smem(const Geom& g, int E, int R);
+
 // Tiles for the one-launch cluster path: as few iterations per warp as keep
 // the tile count within 16.  False when the plan needs more tiles, when the
 // tile's is_token_in_rank rows exceed 64 KB, or when MOE_PLAN_CLUSTER=0.
@@ -744,7 +770,7 @@ bool cluster_geometry(int N, int E, int K, int R, Geom* g) {
     if (static_cast<int64_t>(g->tile_tokens) * R > 65536) return false;
     g->T = static_cast<int>((static_cast<int64_t>(N) + g->tile_tokens - 1) / g->tile_tokens);
     g->C = E + R + 2;
-    return g->T >= 1 && g->T <= kMaxClusterTiles;
+    return g->T >= 1 && g->T <= kMaxClusterTiles && cluster_smem(*g, E, R) <= 220 * 1024;
 }
 
 size_t cluster_smem(const Geom& g, int E, int R) {
@@ -874,7 +900,7 @@ extern "C" MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, in
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        const int big = 200 * 1024;
+        const int big = 220 * 1024;  // the geometry keeps every plan kernel within this
         cudaError_t e1 = cudaFuncSetAttribute(moe::plan_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
         cudaError_t e2 = cudaFuncSetAttribute(moe::plan_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
         cudaError_t e3 = cudaFuncSetAttribute(moe::plan_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
