@@ -51,6 +51,8 @@ SIGNATURES = [
     ("moe_plan_workspace_init", _i32, [_P, _size, _P]),
     ("moe_plan", _i32, [_P, _i32, _i32, _i32, _i32, _i32, _P, _size, ctypes.POINTER(MoePlanOut), _P]),
     ("moe_plan_no_alloc", _i32, [_P, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(MoePlanOut), _P]),
+    ("moe_plan_copy", _i32, [ctypes.POINTER(MoePlanOut), ctypes.POINTER(MoePlanOut), _i32, _i32, _i32, _i32, _i32,
+                             _P]),
     ("moe_plan_balanced", _i32, [ctypes.POINTER(MoePlanOut), _P, _i32, _i32, _i32, _i32, _i32, ctypes.c_int32,
                                  _i32, ctypes.c_int32, ctypes.POINTER(MoeBalancedPlanOut), _P]),
     ("moe_tile_map", _i32, [ctypes.POINTER(MoePlanOut), _i32, _i32, _P, _P, _i64, _P, _P]),

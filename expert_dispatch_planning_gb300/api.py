@@ -110,6 +110,13 @@ class Plan:
             p.dup_loffs, p.dup_counts, p.status)])
         return p
 
+    def clone(self, stream=None) -> "Plan":
+        """A copy of this plan in new buffers (moe_plan_copy)."""
+        c = Plan.allocate(self.N, self.E, self.K, self.R, self.alignment, device=self.dst.device, stream=stream)
+        check("moe_plan_copy", load().moe_plan_copy(ctypes.byref(self.c_struct), ctypes.byref(c.c_struct), self.N,
+                                                   self.E, self.K, self.R, self.alignment, _stream(stream)))
+        return c
+
     def to_host(self) -> dict:
         """Copy every output to numpy (synchronises); dedup arrays cut to their counts."""
         out = {k: getattr(self, k).cpu().numpy() for k in (

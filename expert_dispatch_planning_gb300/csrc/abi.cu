@@ -72,3 +72,44 @@ extern "C" MOE_API int moe_debug_set_plan_fault(int skip_tile, int64_t timeout_n
     g_timeout_ns.store(timeout_ns > 0 ? timeout_ns : 1000000000);
     return MOE_OK;
 }
+
+// Plan reuse (MoonEP MoonEPCommPlan.clone; DeepEP's cached dispatch reuses a
+// plan without planning again): a plan is caller-owned and stays valid for
+// any number of permute / combine calls; this copies one plan into another
+// set of buffers of the same sizes, one asynchronous device copy per array.
+extern "C" MOE_API int moe_plan_copy(const MoePlanOut* src, const MoePlanOut* dst, int N, int E, int K, int R,
+                                     int alignment, cudaStream_t stream) {
+    if (src == nullptr || dst == nullptr || N < 1 || E < 1 || K < 1 || R < 1 || alignment < 1 || E % R != 0)
+        return MOE_ERR_INVALID_ARG;
+    const int64_t p_cap = moe_plan_capacity_rows(N, E, K, alignment);
+    if (p_cap < 0) return MOE_ERR_INVALID_ARG;
+    struct Item {
+        const void* s;
+        void* d;
+        size_t bytes;
+    } items[] = {
+        {src->tokens_per_expert, dst->tokens_per_expert, 4u * E},
+        {src->cu_seqlens, dst->cu_seqlens, 4u * (E + 1)},
+        {src->zero_fill_ranges, dst->zero_fill_ranges, 8u * E},
+        {src->pairs_per_rank, dst->pairs_per_rank, 4u * R},
+        {src->tokens_per_rank, dst->tokens_per_rank, 4u * R},
+        {src->rank_prefix, dst->rank_prefix, 4u * (R + 1)},
+        {src->rank_slot_offsets, dst->rank_slot_offsets, 4u * (R + 1)},
+        {src->is_token_in_rank, dst->is_token_in_rank, static_cast<size_t>(N) * R},
+        {src->dst, dst->dst, 4u * static_cast<size_t>(N) * K},
+        {src->src_of_slot, dst->src_of_slot, 4u * static_cast<size_t>(p_cap)},
+        {src->dup_groups, dst->dup_groups, 12u * static_cast<size_t>(N) * (K / 2)},
+        {src->dup_loffs, dst->dup_loffs, 4u * static_cast<size_t>(N) * (K - 1)},
+        {src->dup_counts, dst->dup_counts, 8u},
+        {src->status, dst->status, 16u},
+    };
+    for (const Item& it : items) {
+        if (it.bytes == 0) continue;
+        if (it.s == nullptr || it.d == nullptr) return MOE_ERR_INVALID_ARG;
+    }
+    for (const Item& it : items) {
+        if (it.bytes == 0) continue;
+        if (cudaMemcpyAsync(it.d, it.s, it.bytes, cudaMemcpyDeviceToDevice, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}

@@ -208,6 +208,16 @@ MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, int R, int al
 MOE_API int moe_plan_no_alloc(const int32_t* topk_idx, int N, int E, int K, int R, int alignment,
                               const MoePlanOut* out, cudaStream_t stream);
 
+/*
+ * Plan reuse (MoonEP MoonEPCommPlan.clone; DeepEP's cached dispatch reuses
+ * a plan instead of planning again).  A plan is caller-owned and stays valid
+ * for any number of moe_permute / moe_combine calls while its buffers live;
+ * this copies plan `src` into the buffers of `dst` (same N, E, K, R,
+ * alignment), one asynchronous device-to-device copy per array on `stream`.
+ */
+MOE_API int moe_plan_copy(const MoePlanOut* src, const MoePlanOut* dst, int N, int E, int K, int R,
+                          int alignment, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- balanced plan */
 /*
  * Capacity-balanced logical-rank plan with redundant experts (MoonEP

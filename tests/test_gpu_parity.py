@@ -341,3 +341,22 @@ def test_end_to_end(m, name):
     ulp = np.maximum(np.abs(o), 2.0 ** -126) * 2.0 ** -7
     assert np.all(np.abs(g - o) <= np.maximum(1e-2, ulp * 1.0001))
     assert np.mean(g != o) < 1e-3
+
+
+def test_plan_reuse_and_copy(m):
+    """A plan serves several permute/combine calls; a copied plan is identical
+    and keeps working after the original's buffers are overwritten."""
+    w, inp, o_idx, o_w, p, want = rows_case(m, "qwen3")
+    rng = np.random.default_rng(17)
+    c = p.clone()
+    assert_plan_equal(c.to_host(), want)
+    p.dst.fill_(0)          # the copy owns its buffers
+    w32 = torch.from_numpy(o_w.astype(np.float32)).to(dev())
+    for it in range(2):
+        x_bits = workloads.make_x_bits(rng, w.N, w.H)
+        perm = m.permute(to_bf16(x_bits), c)
+        o_perm = oracle.permute(x_bits, want["dst"], want["zero_fill_ranges"], w.K, want["P_cap"])
+        assert np.array_equal(bits(perm)[: want["P"]], o_perm[: want["P"]])
+        out = m.combine(perm, w32, c)
+        assert np.array_equal(bits(out), oracle.combine(o_perm, o_w.astype(np.float32), want["dst"]))
+    assert m.get_status(c) == 0
