@@ -402,7 +402,7 @@ def run_ours(args, w):
 
 
 def run_stage(args, w):
-    """Time one stage alone (inputs resident, K launches back to back)."""
+    """Time one stage alone: inputs resident, K replays of a graph of 10 back-to-back calls."""
     import torch
 
     import expert_dispatch_planning_gb300 as m
@@ -424,13 +424,15 @@ def run_stage(args, w):
         fns["permute"] = lambda: m.permute(x, p, out=perm)
         fns["combine"] = lambda: m.combine(perm, wts, p, out=out)
     fn = fns[args.stage]
+    reps = 10  # calls per captured graph, so that graph launches do not bound µs-scale kernels
     gs = torch.cuda.Stream()
     gs.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(gs):
         fn()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=gs):
-            fn()
+            for _ in range(reps):
+                fn()
     torch.cuda.synchronize()
     for _ in range(max(3, args.warmup)):
         g.replay()
@@ -442,7 +444,7 @@ def run_stage(args, w):
     ev[1].record()
     torch.cuda.synchronize()
     assert m.get_status(p) == 0
-    ms = ev[0].elapsed_time(ev[1]) / args.steps
+    ms = ev[0].elapsed_time(ev[1]) / (args.steps * reps)
     P = int(p.cu_seqlens[-1].item())
     ab = algorithmic_bytes(w, P)
     nbytes = ab[args.stage] if args.stage in ab else ab["plan_count"] + ab["plan_scatter"]

@@ -32,8 +32,10 @@
 //     src_info), is_token_in_rank, and the dedup structures in (token,
 //     first k) order;
 //   - -1 into the padding rows and unused capacity of src_of_slot.
+#include <algorithm>
 #include <map>
 #include <mutex>
+#include <string>
 #include <tuple>
 
 #include "moe_common.cuh"
@@ -90,12 +92,14 @@ __device__ __forceinline__ uint64_t pack_flag(uint32_t epoch, uint32_t st, uint3
     return (static_cast<uint64_t>(flag_tag(epoch)) << 32) | (static_cast<uint64_t>(st) << 30) | (v & 0x3fffffffu);
 }
 
-// Exclusive prefix sum of n values (n <= 4096) in shared memory by one CTA
-// of PLAN_THREADS threads: out[0] = 0, out[i+1] = out[i] + in[i].
-// `in` and `out` may not alias; s_warp holds PLAN_WARPS + 1 ints.
+// Exclusive prefix sum of n values in shared memory by one CTA of WARPS
+// warps: out[0] = 0, out[i+1] = out[i] + in[i].  `in` and `out` may not
+// alias; s_warp holds WARPS + 1 ints.
+template <int WARPS>
 __device__ void block_exclusive_scan(const int32_t* in, int n, int32_t* out, int32_t* s_warp) {
+    constexpr int THREADS = WARPS * 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int chunk = (n + PLAN_THREADS - 1) / PLAN_THREADS;
+    const int chunk = (n + THREADS - 1) / THREADS;
     const int b = min(n, tid * chunk), e = min(n, b + chunk);
     int32_t local = 0;
     for (int i = b; i < e; ++i) local += in[i];
@@ -107,16 +111,16 @@ __device__ void block_exclusive_scan(const int32_t* in, int n, int32_t* out, int
     }
     if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
-    if (warp == 0) {  // exclusive scan of the 16 warp totals
-        const int32_t v = lane < PLAN_WARPS ? s_warp[lane] : 0;
+    if (warp == 0) {  // exclusive scan of the warp totals
+        const int32_t v = lane < WARPS ? s_warp[lane] : 0;
         int32_t w_incl = v;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const int32_t y = __shfl_up_sync(FULL_MASK, w_incl, off);
             if (lane >= off) w_incl += y;
         }
-        if (lane < PLAN_WARPS) s_warp[lane] = w_incl - v;
-        if (lane == PLAN_WARPS - 1) s_warp[PLAN_WARPS] = w_incl;
+        if (lane < WARPS) s_warp[lane] = w_incl - v;
+        if (lane == WARPS - 1) s_warp[WARPS] = w_incl;
     }
     __syncthreads();
     int32_t run = s_warp[warp] + incl - local;
@@ -124,7 +128,7 @@ __device__ void block_exclusive_scan(const int32_t* in, int n, int32_t* out, int
         out[i] = run;
         run += in[i];
     }
-    if (tid == 0) out[n] = s_warp[PLAN_WARPS];
+    if (tid == 0) out[n] = s_warp[WARPS];
     __syncthreads();
 }
 
@@ -134,27 +138,29 @@ __device__ void block_exclusive_scan(const int32_t* in, int n, int32_t* out, int
 // when `write`, every totals-derived output (MoonEP per-rank cu_seqlens and
 // zero_fill_ranges with padded = round_up(count, alignment) for count > 0;
 // DeepEP notify_dispatch rank prefix).  s_pad: E + R + 2 ints of scratch.
-// Contains __syncthreads: every thread of the CTA calls it.
+// Contains __syncthreads: every thread of the CTA (WARPS warps) calls it.
+template <int WARPS>
 __device__ void plan_totals(const PlanArgs& a, const int32_t* s_tot, int32_t* s_pad, int32_t* s_cu, int32_t* s_warp,
                             bool write) {
+    constexpr int THREADS = WARPS * 32;
     const int tid = threadIdx.x;
     const int E = a.E, R = a.R, al = a.alignment;
-    for (int e = tid; e < E; e += PLAN_THREADS) {
+    for (int e = tid; e < E; e += THREADS) {
         const int32_t c = s_tot[e];
         s_pad[e] = c > 0 ? static_cast<int32_t>((static_cast<int64_t>(c) + al - 1) / al * al) : 0;
     }
     __syncthreads();
-    block_exclusive_scan(s_pad, E, s_cu, s_warp);  // s_cu[0..E] = cu
+    block_exclusive_scan<WARPS>(s_pad, E, s_cu, s_warp);  // s_cu[0..E] = cu
     if (!write) return;
-    for (int e = tid; e < E; e += PLAN_THREADS) {
+    for (int e = tid; e < E; e += THREADS) {
         a.out.tokens_per_expert[e] = s_tot[e];
         const int32_t pad = s_pad[e] - s_tot[e];
         a.out.zero_fill_ranges[2 * e] = pad > 0 ? s_cu[e] + s_tot[e] : 0;
         a.out.zero_fill_ranges[2 * e + 1] = pad > 0 ? pad : 0;
     }
-    for (int e = tid; e <= E; e += PLAN_THREADS) a.out.cu_seqlens[e] = s_cu[e];
-    for (int r = tid; r <= R; r += PLAN_THREADS) a.out.rank_slot_offsets[r] = s_cu[r * a.epn];
-    for (int r = tid; r < R; r += PLAN_THREADS) {
+    for (int e = tid; e <= E; e += THREADS) a.out.cu_seqlens[e] = s_cu[e];
+    for (int r = tid; r <= R; r += THREADS) a.out.rank_slot_offsets[r] = s_cu[r * a.epn];
+    for (int r = tid; r < R; r += THREADS) {
         int32_t pairs = 0;
         for (int e = r * a.epn; e < (r + 1) * a.epn; ++e) pairs += s_tot[e];
         a.out.pairs_per_rank[r] = pairs;
@@ -165,8 +171,8 @@ __device__ void plan_totals(const PlanArgs& a, const int32_t* s_tot, int32_t* s_
         a.out.dup_counts[1] = s_tot[E + R + 1];
     }
     __syncthreads();
-    block_exclusive_scan(s_tot + E, R, s_pad, s_warp);  // s_pad[0..R] = rank prefix
-    for (int r = tid; r <= R; r += PLAN_THREADS) a.out.rank_prefix[r] = s_pad[r];
+    block_exclusive_scan<WARPS>(s_tot + E, R, s_pad, s_warp);  // s_pad[0..R] = rank prefix
+    for (int r = tid; r <= R; r += THREADS) a.out.rank_prefix[r] = s_pad[r];
 }
 
 // Per-pair results of a tile's first pass, kept in shared memory (8 bytes
@@ -281,44 +287,47 @@ __device__ __noinline__ void tile_phase1(const PlanArgs& a, int tile, int32_t* s
 
 // Exclusive scan of the per-warp-run values by one warp (lane w holds warp
 // run w's value), written back with `base` added.
+template <int WARPS>
 __device__ __forceinline__ void warp_scan_runs(int32_t* s_val, int32_t base) {
     const int lane = threadIdx.x & 31;
-    int32_t v = lane < PLAN_WARPS ? s_val[lane] : 0;
+    int32_t v = lane < WARPS ? s_val[lane] : 0;
     int32_t incl = v;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         const int32_t y = __shfl_up_sync(FULL_MASK, incl, off);
         if (lane >= off) incl += y;
     }
-    if (lane < PLAN_WARPS) s_val[lane] = base + incl - v;
+    if (lane < WARPS) s_val[lane] = base + incl - v;
 }
 
 // Second pass over a tile, after the bases are known: s_base[e] = first slot
 // of expert e in this tile, g_base / d_base = groups / duplicates of earlier
 // tiles.  Turns the per-warp counts into per-warp bases, then writes dst,
 // src_of_slot, dup_groups, dup_loffs and the tile's is_token_in_rank rows.
+template <int WARPS>
 __device__ __noinline__ void tile_phase3(const PlanArgs& a, int tile, const int32_t* s_base, int32_t g_base,
                                          int32_t d_base, int32_t* s_wc, int32_t* s_wg, int32_t* s_wd,
                                          const uint8_t* s_itr, const uint2* s_items) {
+    constexpr int THREADS = WARPS * 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int E = a.E, K = a.K, R = a.R;
     const int64_t tok0 = static_cast<int64_t>(tile) * a.tile_tokens;
     // per (warp run, expert): the expert's pairs in earlier warp runs; a
     // thread per expert (neighbouring threads, neighbouring banks), all its
     // loads issued before the running sum
-    for (int e = tid; e < E; e += PLAN_THREADS) {
-        int32_t v[PLAN_WARPS];
+    for (int e = tid; e < E; e += THREADS) {
+        int32_t v[WARPS];
 #pragma unroll
-        for (int w = 0; w < PLAN_WARPS; ++w) v[w] = s_wc[w * E + e];
+        for (int w = 0; w < WARPS; ++w) v[w] = s_wc[w * E + e];
         int32_t run = s_base[e];
 #pragma unroll
-        for (int w = 0; w < PLAN_WARPS; ++w) {
+        for (int w = 0; w < WARPS; ++w) {
             s_wc[w * E + e] = run;
             run += v[w];
         }
     }
-    if (warp == PLAN_WARPS - 1) warp_scan_runs(s_wg, g_base);
-    if (warp == PLAN_WARPS - 2) warp_scan_runs(s_wd, d_base);
+    if (warp == WARPS - 1) warp_scan_runs<WARPS>(s_wg, g_base);
+    if (warp == WARPS - 2) warp_scan_runs<WARPS>(s_wd, d_base);
     __syncthreads();
 
     const int tok_in_iter = lane / K, k = lane - (lane / K) * K;
@@ -366,23 +375,25 @@ __device__ __noinline__ void tile_phase3(const PlanArgs& a, int tile, const int3
     uint8_t* g = a.out.is_token_in_rank + tok0 * R;
     if ((reinterpret_cast<uintptr_t>(g) & 15u) == 0) {
         const int64_t nvec = nbytes / 16;
-        for (int64_t v = tid; v < nvec; v += PLAN_THREADS)
+        for (int64_t v = tid; v < nvec; v += THREADS)
             reinterpret_cast<uint4*>(g)[v] = reinterpret_cast<const uint4*>(s_itr)[v];
-        for (int64_t b = nvec * 16 + tid; b < nbytes; b += PLAN_THREADS) g[b] = s_itr[b];
+        for (int64_t b = nvec * 16 + tid; b < nbytes; b += THREADS) g[b] = s_itr[b];
     } else {
-        for (int64_t b = tid; b < nbytes; b += PLAN_THREADS) g[b] = s_itr[b];
+        for (int64_t b = tid; b < nbytes; b += THREADS) g[b] = s_itr[b];
     }
 }
 
 // -1 into src_of_slot for the padding rows of experts tile, tile + T, ...
 // (cu, cnt: cu_seqlens and per-expert counts) and for this tile's share of
 // the unused rows [P, P_cap).
+template <int WARPS>
 __device__ __forceinline__ void fill_unused(const PlanArgs& a, int tile, int T, const int32_t* cu, const int32_t* cnt) {
+    constexpr int THREADS = WARPS * 32;
     const int tid = threadIdx.x;
     const int per = a.alignment - 1;  // at most this many padding rows per expert
     if (per > 0) {
         const int mine = (a.E - tile + T - 1) / T;  // experts tile, tile + T, ...
-        for (int i = tid; i < mine * per; i += PLAN_THREADS) {
+        for (int i = tid; i < mine * per; i += THREADS) {
             const int e = tile + (i / per) * T, j = i - (i / per) * per;
             const int32_t start = cu[e] + cnt[e];
             if (j < cu[e + 1] - start && start >= 0 && static_cast<int64_t>(start) + j < a.p_cap)
@@ -393,7 +404,7 @@ __device__ __forceinline__ void fill_unused(const PlanArgs& a, int tile, int T, 
     const int64_t rest = a.p_cap - P;
     const int64_t share = (rest + T - 1) / T;
     const int64_t b = P + share * tile, e = min(a.p_cap, b + share);
-    for (int64_t j = b + tid; j < e; j += PLAN_THREADS) a.out.src_of_slot[j] = -1;
+    for (int64_t j = b + tid; j < e; j += THREADS) a.out.src_of_slot[j] = -1;
 }
 
 // ---------------------------------------------------------------- launch 1
@@ -524,7 +535,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_count_kernel(const PlanArgs
         __syncthreads();
 
         // ---- last tile: totals -> aligned offsets and rank arrays
-        if (tile == a.T - 1 && tile != a.skip_tile && s_err == 0) plan_totals(a, s_tot, s_tmp, s_scan, s_warp, true);
+        if (tile == a.T - 1 && tile != a.skip_tile && s_err == 0) plan_totals<PLAN_WARPS>(a, s_tot, s_tmp, s_scan, s_warp, true);
     }
 
     // ---- completion: the last CTA to finish closes the epoch
@@ -572,8 +583,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_scatter_kernel(const PlanAr
     for (int e = tid; e < E; e += PLAN_THREADS) s_base[e] = __ldg(a.out.cu_seqlens + e) + __ldg(tp + e);
     const int32_t g_base = __ldg(tp + E + R), d_base = __ldg(tp + E + R + 1);
     __syncthreads();
-    tile_phase3(a, tile, s_base, g_base, d_base, s_wc, s_wg, s_wd, s_itr, s_items);
-    fill_unused(a, tile, a.T, a.out.cu_seqlens, a.out.tokens_per_expert);
+    tile_phase3<PLAN_WARPS>(a, tile, s_base, g_base, d_base, s_wc, s_wg, s_wd, s_itr, s_items);
+    fill_unused<PLAN_WARPS>(a, tile, a.T, a.out.cu_seqlens, a.out.tokens_per_expert);
 }
 
 // ---------------------------------------------------------------- cluster path
@@ -588,6 +599,9 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
     return r;
 }
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 // Address of `p` (this CTA's shared memory) in the shared memory of CTA
 // `rank` of the cluster, then a load from it.
@@ -673,12 +687,503 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_cluster_kernel(const PlanAr
     cluster_arrive();  // done reading the other CTAs' shared memory
     __syncthreads();
 
-    plan_totals(a, s_tot, s_pad, s_cu, s_warp, rank == 0);
+    plan_totals<PLAN_WARPS>(a, s_tot, s_pad, s_cu, s_warp, rank == 0);
     for (int e = tid; e < E; e += PLAN_THREADS) s_base[e] += s_cu[e];
     __syncthreads();
-    tile_phase3(a, tile, s_base, s_gd[0], s_gd[1], s_wc, s_wg, s_wd, s_itr, s_items);
-    fill_unused(a, tile, static_cast<int>(ncta), s_cu, s_tot);
+    tile_phase3<PLAN_WARPS>(a, tile, s_base, s_gd[0], s_gd[1], s_wc, s_wg, s_wd, s_itr, s_items);
+    fill_unused<PLAN_WARPS>(a, tile, static_cast<int>(ncta), s_cu, s_tot);
     cluster_wait();  // keep this CTA's shared memory alive until all reads are done
+}
+
+// ---------------------------------------------------------------- small-E path
+// E <= 32 and R <= 32 (NB = 3 bits for E, R <= 8, else 5): one
+// thread-block cluster of T <= 16 CTAs of 32 warps, IPT warp steps per warp.
+// Per warp step, ballots of the NB bits of each pair's expert (and, among the
+// first pairs of their (token, rank), of its rank) give every lane x the
+// lanes holding expert x (rank x) with one LOP per bit, so lane x owns the
+// running counts of expert x and rank x; match.any gives a pair's rank among
+// same-expert pairs and the (token, rank) duplicate test, and the token's
+// rank bitmask is written straight to is_token_in_rank.  One CTA barrier
+// turns the per-warp counts into warp bases (lanes split over experts and
+// warps, xor-shuffle sums); each CTA then pushes its tile's counts into the
+// shared memory of every CTA of the cluster (remote stores, no round trip),
+// and after one cluster barrier every warp derives the tile prefixes, the
+// totals and cu_seqlens from its own shared memory and writes its pairs'
+// slots.  Tile 0's warp 0 writes the totals-derived outputs.  Per-pair
+// results stay in registers.
+constexpr int SMALL_MAX = 32;
+
+__device__ __forceinline__ void st_dsmem_s32(uint32_t addr, int32_t v) {
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int warp_incl_scan(int v, int width) {
+    const int lane = threadIdx.x & 31;
+    for (int off = 1; off < width; off <<= 1) {
+        const int y = __shfl_up_sync(FULL_MASK, v, off);
+        if (lane >= off) v += y;
+    }
+    return v;
+}
+
+// is_token_in_rank row of one token from its rank bitmask (bytes 0 / 1).
+__device__ __forceinline__ void store_rank_row(uint8_t* row, uint32_t mask, int R) {
+    if ((R & 3) == 0 && (reinterpret_cast<uintptr_t>(row) & 3u) == 0) {
+        for (int c = 0; c < R / 4; ++c) {
+            const uint32_t m = mask >> (4 * c);
+            reinterpret_cast<uint32_t*>(row)[c] = (m & 1u) | ((m & 2u) << 7) | ((m & 4u) << 14) | ((m & 8u) << 21);
+        }
+    } else {
+        for (int x = 0; x < R; ++x) row[x] = static_cast<uint8_t>((mask >> x) & 1u);
+    }
+}
+
+template <int IPT, int NB>
+__global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs a) {
+    constexpr int EP = 1 << NB;         // experts (and ranks) a lane group covers
+    constexpr int CHUNKS = 32 / EP;     // lane groups per warp
+    constexpr int CW = 2 * EP + 2;      // tile columns: experts, ranks, groups, duplicates
+    constexpr int TPC = 16 / CHUNKS;    // tiles per lane group in the cross-tile sums
+    __shared__ int32_t s_wc[PLAN_WARPS][EP + 1];  // per-warp pairs per expert (+1: no bank conflicts)
+    __shared__ int32_t s_wr[PLAN_WARPS][EP + 1];  // per-warp tokens per rank
+    __shared__ int32_t s_wg[PLAN_WARPS], s_wd[PLAN_WARPS];
+    __shared__ int32_t s_cnt[CW];                 // this tile's counts
+    __shared__ int32_t s_all[16][CW];             // every tile's counts, pushed by its CTA
+
+    pdl_wait();
+    pdl_trigger();
+    cluster_arrive_relaxed();  // this CTA has started: the others may push into it once all have
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int E = a.E, K = a.K, R = a.R;
+    const uint32_t crank = cluster_ctarank(), ncta = cluster_nctarank();
+    const int tile = static_cast<int>(crank);
+    const int64_t tok0 = static_cast<int64_t>(tile) * a.tile_tokens;
+    const unsigned lt = (1u << lane) - 1u;
+    const int act = a.tpw * K;
+    const int tok_in_iter = lane / K, k = lane - tok_in_iter * K;
+    const int tok_lane0 = tok_in_iter * K;
+    const unsigned below_tok = (1u << tok_lane0) - 1u;
+    const unsigned seg = (K >= 32 ? FULL_MASK : ((1u << K) - 1u)) << tok_lane0;  // the token's lanes
+    const bool k_pow2 = (K & (K - 1)) == 0;
+    unsigned xl[NB];  // bit b of this lane's index, as an all-ones / all-zeros word
+#pragma unroll
+    for (int b = 0; b < NB; ++b) xl[b] = 0u - ((static_cast<unsigned>(lane) >> b) & 1u);
+
+    int ids[IPT];
+#pragma unroll
+    for (int i = 0; i < IPT; ++i) {
+        const int64_t s = tok0 + static_cast<int64_t>(warp * IPT + i) * a.tpw + tok_in_iter;
+        ids[i] = (lane < act && s < a.N) ? __ldg(a.topk + s * K + k) : -1;
+    }
+
+    // ---- first pass, all in registers
+    int cnt_e = 0, cnt_r = 0, run_g = 0, run_d = 0;  // lane x: pairs of expert x / tokens on rank x so far
+    uint2 item[IPT];
+#pragma unroll
+    for (int i = 0; i < IPT; ++i) {
+        const int64_t s = tok0 + static_cast<int64_t>(warp * IPT + i) * a.tpw + tok_in_iter;
+        bool active = lane < act && s < a.N;
+        int e = 0;
+        if (active) {
+            e = ids[i];
+            if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
+                record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(s * K + k));
+                active = false;
+                e = 0;
+            }
+        }
+        // bit b of every lane's expert and rank, one ballot each; lanes
+        // holding a given value are the AND of matching bit words
+        const unsigned amask = __ballot_sync(FULL_MASK, active);
+        const int r = rank_of(a, e);
+        unsigned me = amask, peers = amask, mr = amask, pr = amask;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const unsigned eb = __ballot_sync(FULL_MASK, (e >> b) & 1);
+            const unsigned rb = __ballot_sync(FULL_MASK, (r >> b) & 1);
+            me &= ~(eb ^ xl[b]);                   // lanes holding expert `lane`
+            peers &= ~(eb ^ (0u - ((e >> b) & 1)));  // lanes holding this lane's expert
+            mr &= ~(rb ^ xl[b]);                   // lanes on rank `lane`
+            pr &= ~(rb ^ (0u - ((r >> b) & 1)));     // lanes on this lane's rank
+        }
+        const int wr = __popc(peers & lt) + __shfl_sync(FULL_MASK, cnt_e, e);
+        cnt_e += __popc(me);
+
+        const unsigned pd = pr & seg;  // this token's pairs on this lane's rank
+        const bool prim = active && (pd & lt) == 0u;
+        const bool dup = active && !prim;
+        const bool opens = prim && __popc(pd) >= 2;
+        const unsigned pmask = __ballot_sync(FULL_MASK, prim);
+        cnt_r += __popc(mr & pmask);  // tokens on rank `lane`
+        const unsigned gball = __ballot_sync(FULL_MASK, opens);
+        const unsigned dball = amask & ~pmask;
+        // duplicates of a token: group after group (groups in order of their
+        // primary lane), k order inside a group; a warp scan of the group
+        // sizes gives the duplicates of the groups opening before a lane
+        const int my_p = __ffs(pd) - 1;
+        const int gsz = opens ? __popc(pd) - 1 : 0;
+        const int excl = warp_incl_scan(gsz, 32) - gsz;
+        const int tok_base = __shfl_sync(FULL_MASK, excl, tok_lane0 & 31);
+        const int groups_before = __shfl_sync(FULL_MASK, excl, my_p & 31) - tok_base;
+        const int before = groups_before + (dup ? __popc(pd & lt) - 1 : 0);
+        const int dup_pos = run_d + __popc(dball & below_tok) + before;
+
+        // the token's rank bitmask: OR over its K lanes
+        uint32_t rbits = prim ? 1u << r : 0u;
+        if (k_pow2) {
+            for (int off = 1; off < K; off <<= 1) rbits |= __shfl_xor_sync(FULL_MASK, rbits, off);
+        } else {
+            uint32_t acc = 0;
+            for (int q = 0; q < K; ++q) acc |= __shfl_sync(FULL_MASK, rbits, (tok_lane0 + q) & 31);
+            rbits = acc;
+        }
+        if (active && k == 0) store_rank_row(a.out.is_token_in_rank + s * R, rbits, R);
+
+        item[i] = active ? pack_item(e, wr, dup, opens, __popc(pd) - 1, opens ? run_g + __popc(gball & lt) : dup_pos,
+                                     dup_pos)
+                         : make_uint2(ITEM_NONE, 0u);
+        run_g += __popc(gball);
+        run_d += __popc(dball);
+    }
+    if (lane < EP) {
+        s_wc[warp][lane] = cnt_e;
+        s_wr[warp][lane] = cnt_r;
+    }
+    if (lane == 0) {
+        s_wg[warp] = run_g;
+        s_wd[warp] = run_d;
+    }
+    __syncthreads();
+    cluster_wait();  // every CTA of the cluster has started
+
+    // ---- warp bases: lane l sums expert (l mod EP) over warps
+    // [(l / EP) * EP, +EP), then xor-shuffles add the lane groups
+    const int x = lane & (EP - 1), chunk = lane / EP;
+    int base_e = 0, tile_e = 0;
+    {
+        int v[EP];
+#pragma unroll
+        for (int j = 0; j < EP; ++j) v[j] = s_wc[chunk * EP + j][x];
+#pragma unroll
+        for (int j = 0; j < EP; ++j) {
+            base_e += chunk * EP + j < warp ? v[j] : 0;
+            tile_e += v[j];
+        }
+#pragma unroll
+        for (int off = EP; off < 32; off <<= 1) {
+            base_e += __shfl_xor_sync(FULL_MASK, base_e, off);
+            tile_e += __shfl_xor_sync(FULL_MASK, tile_e, off);
+        }
+    }
+    const int vg = s_wg[lane], vd = s_wd[lane];  // PLAN_WARPS == 32
+    const int g_wbase = __reduce_add_sync(FULL_MASK, lane < warp ? vg : 0);
+    const int d_wbase = __reduce_add_sync(FULL_MASK, lane < warp ? vd : 0);
+
+    // ---- warp 0: the tile's counts, pushed into every CTA's s_all[tile]
+    if (warp == 0) {
+        int tile_r = 0;
+        {
+            int v[EP];
+#pragma unroll
+            for (int j = 0; j < EP; ++j) v[j] = s_wr[chunk * EP + j][x];
+#pragma unroll
+            for (int j = 0; j < EP; ++j) tile_r += v[j];
+#pragma unroll
+            for (int off = EP; off < 32; off <<= 1) tile_r += __shfl_xor_sync(FULL_MASK, tile_r, off);
+        }
+        const int g_tile = __reduce_add_sync(FULL_MASK, vg), d_tile = __reduce_add_sync(FULL_MASK, vd);
+        if (lane < EP) {
+            s_cnt[lane] = tile_e;
+            s_cnt[EP + lane] = tile_r;
+        }
+        if (lane == 0) {
+            s_cnt[2 * EP] = g_tile;
+            s_cnt[2 * EP + 1] = d_tile;
+        }
+        __syncwarp();
+        for (int idx = lane; idx < static_cast<int>(ncta) * CW; idx += 32) {
+            const int q = idx / CW, c = idx - q * CW;
+            st_dsmem_s32(dsmem_addr(&s_all[tile][c], static_cast<uint32_t>(q)), s_cnt[c]);
+        }
+    }
+    cluster_arrive();  // release: this CTA's pushes
+    cluster_wait();    // acquire: every tile's counts are in s_all
+
+    // ---- lower tiles and totals, every warp from its own shared memory
+    int pre_e = 0, tot_e = 0;
+    {
+#pragma unroll
+        for (int j = 0; j < TPC; ++j) {
+            const int q = chunk * TPC + j;
+            const int v = q < static_cast<int>(ncta) ? s_all[q][x] : 0;
+            pre_e += q < tile ? v : 0;
+            tot_e += v;
+        }
+#pragma unroll
+        for (int off = EP; off < 32; off <<= 1) {
+            pre_e += __shfl_xor_sync(FULL_MASK, pre_e, off);
+            tot_e += __shfl_xor_sync(FULL_MASK, tot_e, off);
+        }
+    }
+    int gq = 0, dq = 0;
+    if (static_cast<uint32_t>(lane) < ncta) {
+        gq = s_all[lane][2 * EP];
+        dq = s_all[lane][2 * EP + 1];
+    }
+    const int g_pre = __reduce_add_sync(FULL_MASK, lane < tile ? gq : 0);
+    const int d_pre = __reduce_add_sync(FULL_MASK, lane < tile ? dq : 0);
+
+    const unsigned al = static_cast<unsigned>(a.alignment);
+    int padded = 0;
+    if (lane < E && tot_e > 0) {
+        const unsigned t = static_cast<unsigned>(tot_e) + al - 1u;
+        padded = static_cast<int>((al & (al - 1u)) == 0u ? (t & ~(al - 1u)) : t / al * al);
+    }
+    const int cu_incl = warp_incl_scan(padded, EP);
+    const int cu_e = cu_incl - padded;
+    const int P = __shfl_sync(FULL_MASK, cu_incl, EP - 1);
+    const int slot_base = cu_e + pre_e + base_e;  // first slot of expert `lane` in this warp run
+
+    // ---- second pass: slots, dst, src_of_slot, dedup structures
+    const int64_t gbase = static_cast<int64_t>(g_pre) + g_wbase, dbase = static_cast<int64_t>(d_pre) + d_wbase;
+#pragma unroll
+    for (int i = 0; i < IPT; ++i) {
+        const uint2 it = item[i];
+        const uint32_t e = it.x & 0x7ffu;
+        const int sb = __shfl_sync(FULL_MASK, slot_base, static_cast<int>(e & 31u));
+        if (e == ITEM_NONE) continue;
+        const int64_t s = tok0 + static_cast<int64_t>(warp * IPT + i) * a.tpw + tok_in_iter;
+        const int64_t f = s * K + k;
+        const int32_t slot = sb + static_cast<int32_t>((it.x >> 11) & 0x3ffu);
+        if (slot < 0 || static_cast<int64_t>(slot) >= a.p_cap) {
+            record_error(a.out.status, MOE_ERR_DEVICE_INDEX, slot);
+            continue;
+        }
+        const bool dup = (it.x >> 21) & 1u;
+        const bool opens = (it.x >> 22) & 1u;
+        const int32_t ia = static_cast<int32_t>(it.y & 0xffffu), ib = static_cast<int32_t>(it.y >> 16);
+        a.out.dst[f] = dup ? -slot - 1 : slot;
+        a.out.src_of_slot[slot] = static_cast<int32_t>(f);
+        if (opens) {
+            const int64_t g = gbase + ia;
+            if (g >= static_cast<int64_t>(a.N) * (K / 2)) {
+                record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(g));
+                continue;
+            }
+            int32_t* row = a.out.dup_groups + 3 * g;
+            row[0] = slot;
+            row[1] = static_cast<int32_t>(dbase + ib);
+            row[2] = static_cast<int32_t>(it.x >> 23);
+        } else if (dup) {
+            const int64_t pos = dbase + ia;
+            if (pos >= static_cast<int64_t>(a.N) * (K - 1)) {
+                record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(pos));
+                continue;
+            }
+            a.out.dup_loffs[pos] = slot;
+        }
+    }
+
+    // ---- totals-derived outputs (MoonEP cu_seqlens / zero_fill_ranges;
+    // DeepEP notify_dispatch rank prefix)
+    if (tile == 0 && warp == 0) {
+        int tot_r = 0;
+#pragma unroll
+        for (int j = 0; j < TPC; ++j) {
+            const int q = chunk * TPC + j;
+            tot_r += q < static_cast<int>(ncta) ? s_all[q][EP + x] : 0;
+        }
+#pragma unroll
+        for (int off = EP; off < 32; off <<= 1) tot_r += __shfl_xor_sync(FULL_MASK, tot_r, off);
+        if (lane >= R) tot_r = 0;
+        const int32_t g_tot = __reduce_add_sync(FULL_MASK, gq), d_tot = __reduce_add_sync(FULL_MASK, dq);
+        const int epn = a.epn;
+        const int rso = __shfl_sync(FULL_MASK, cu_e, (lane * epn) & 31);
+        int ppr = 0;
+        for (int j = 0; j < epn; ++j) ppr += __shfl_sync(FULL_MASK, tot_e, (lane * epn + j) & 31);
+        const int tpr_incl = warp_incl_scan(tot_r, 32);
+        const int tpr_total = __shfl_sync(FULL_MASK, tpr_incl, 31);
+        if (lane < E) {
+            a.out.tokens_per_expert[lane] = tot_e;
+            a.out.cu_seqlens[lane] = cu_e;
+            const int pad = padded - tot_e;
+            a.out.zero_fill_ranges[2 * lane] = pad > 0 ? cu_e + tot_e : 0;
+            a.out.zero_fill_ranges[2 * lane + 1] = pad > 0 ? pad : 0;
+        }
+        if (lane < R) {
+            a.out.rank_slot_offsets[lane] = rso;
+            a.out.pairs_per_rank[lane] = ppr;
+            a.out.tokens_per_rank[lane] = tot_r;
+            a.out.rank_prefix[lane] = tpr_incl - tot_r;
+        }
+        if (lane == 0) {
+            a.out.cu_seqlens[E] = P;
+            a.out.rank_slot_offsets[R] = P;
+            a.out.rank_prefix[R] = tpr_total;
+            a.out.dup_counts[0] = g_tot;
+            a.out.dup_counts[1] = d_tot;
+        }
+    }
+
+    // ---- -1 into the padding rows (warp w: expert w, on tiles w mod T)
+    // and into this tile's share of the unused rows [P, P_cap)
+    if (warp < E && static_cast<uint32_t>(warp) % ncta == crank) {
+        const int start = __shfl_sync(FULL_MASK, cu_e + tot_e, warp);
+        const int end = __shfl_sync(FULL_MASK, cu_incl, warp);
+        for (int j = start + lane; j < end; j += 32)
+            if (j >= 0 && static_cast<int64_t>(j) < a.p_cap) a.out.src_of_slot[j] = -1;
+    }
+    {
+        const uint32_t cap = static_cast<uint32_t>(a.p_cap);  // < 2^31
+        const uint32_t rest = cap - static_cast<uint32_t>(P);
+        const uint32_t share = (rest + ncta - 1u) / ncta;
+        const uint32_t b = static_cast<uint32_t>(P) + share * crank, e = min(cap, b + share);
+        for (uint32_t j = b + tid; j < e; j += PLAN_THREADS) a.out.src_of_slot[j] = -1;
+    }
+}
+
+// ---------------------------------------------------------------- grid path
+// The whole plan in one launch of T <= 152 CTAs of WARPS warps, all resident
+// at once (the host checks the occupancy), one tile each.  Each CTA runs its
+// tile's first pass and publishes the column counts column-major
+// (counts[c][tile]) followed by one epoch-tagged flag word; then it waits
+// (bounded in time) until every tile's flag carries the running call's tag
+// and reduces every tile's counts itself: the sum over lower tiles is its
+// exclusive prefix, the sum over all the totals.  Every CTA scans the totals
+// into cu_seqlens, tile 0 writes the totals-derived outputs, and the tile's
+// second pass writes the slots.  The last CTA to finish closes the epoch.
+// Compared with the cluster path the work is spread over all SMs; compared
+// with the look-back path there is no chain of waits and one launch.
+template <int WARPS>
+__global__ void __launch_bounds__(WARPS * 32) plan_grid_kernel(const PlanArgs a) {
+    constexpr int THREADS = WARPS * 32;
+    extern __shared__ __align__(16) int32_t s_dyn[];
+    const int E = a.E, R = a.R, C = a.C, T = a.T;
+    uint2* s_items = reinterpret_cast<uint2*>(s_dyn);  // [WARPS][ipt][32]
+    int32_t* s_wc = s_dyn + 2 * WARPS * 32 * a.ipt;     // [WARPS][E]
+    int32_t* s_cnt = s_wc + WARPS * E;                  // [C]  this tile's column counts
+    int32_t* s_tot = s_cnt + C;                         // [C]  totals over all tiles
+    int32_t* s_excl = s_tot + C;                        // [C]  sums over lower tiles
+    int32_t* s_pad = s_excl + C;                        // [E + R + 2]
+    int32_t* s_cu = s_pad + E + R + 2;                  // [E + R + 2]
+    uint8_t* s_itr = align16_after(s_dyn, s_cu + E + R + 2);  // [tile_tokens][R]
+    __shared__ int32_t s_wg[WARPS], s_wd[WARPS], s_warp[WARPS + 1];
+    __shared__ uint32_t s_epoch;
+    __shared__ int s_bad;
+
+    pdl_wait();
+    pdl_trigger();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tile = blockIdx.x;
+    if (tid == 0) {
+        // the ticket only validates the header: a workspace that was never
+        // zeroed hands out an id outside [0, T) to some CTA
+        const uint32_t ticket = atomicAdd(&a.hdr->ticket, 1u);
+        s_epoch = (*reinterpret_cast<volatile uint32_t*>(&a.hdr->epoch) + 1u) & 0x7fffffffu;
+        s_bad = ticket >= static_cast<uint32_t>(T) ? 1 : 0;
+        if (s_bad) record_error(a.out.status, MOE_ERR_WORKSPACE, static_cast<int>(ticket));
+    }
+    const int itr_bytes = a.tile_tokens * R;
+    for (int i = tid; i < WARPS * E; i += THREADS) s_wc[i] = 0;
+    for (int i = tid; i < (itr_bytes + 3) / 4; i += THREADS) reinterpret_cast<int32_t*>(s_itr)[i] = 0;
+    for (int c = E + tid; c < C; c += THREADS) s_cnt[c] = 0;
+    __syncthreads();
+    const uint32_t epoch = s_epoch;
+
+    tile_phase1(a, tile, s_wc, s_itr, s_wg, s_wd, s_cnt + E, s_items);
+    __syncthreads();
+    for (int e = tid; e < E; e += THREADS) {
+        int32_t v[WARPS];
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) v[w] = s_wc[w * E + e];
+        int32_t c = 0;
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) c += v[w];
+        s_cnt[e] = c;
+    }
+    if (warp == 0) {
+        const int32_t g = __reduce_add_sync(FULL_MASK, lane < WARPS ? s_wg[lane] : 0);
+        const int32_t d = __reduce_add_sync(FULL_MASK, lane < WARPS ? s_wd[lane] : 0);
+        if (lane == 0) {
+            s_cnt[E + R] = g;
+            s_cnt[E + R + 1] = d;
+        }
+    }
+    __syncthreads();
+
+    // ---- publish: counts, then the flag (every writer fences before the
+    // barrier, so the flag store is ordered after all of them)
+    int32_t* counts = a.tile_prefix;  // [C][T]
+    for (int c = tid; c < C; c += THREADS) {
+        st_relaxed_s32(counts + static_cast<size_t>(c) * T + tile, s_cnt[c]);
+        __threadfence();
+    }
+    __syncthreads();
+    if (tid == 0 && tile != a.skip_tile)
+        st_relaxed_u64(a.flags + tile, pack_flag(epoch, s_bad ? ST_ERR : ST_PRE, 0u));
+
+    // ---- wait for every tile's flag (a thread per tile; T <= THREADS)
+    if (tid < T) {
+        uint64_t t0 = 0;
+        while (true) {
+            const uint64_t w = ld_relaxed_u64(a.flags + tid);
+            if (static_cast<uint32_t>(w >> 32) == flag_tag(epoch)) {
+                if (((static_cast<uint32_t>(w) >> 30) & 3u) == ST_ERR) s_bad = 1;
+                break;
+            }
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > static_cast<uint64_t>(a.timeout_ns)) {
+                record_error(a.out.status, MOE_ERR_DEVICE_TIMEOUT, tile);
+                s_bad = 1;
+                break;
+            }
+            __nanosleep(64);
+        }
+        __threadfence();  // acquire: the counts behind the flag are read below
+    }
+    __syncthreads();
+
+    if (!s_bad) {  // uniform across the CTA
+        // ---- every tile's counts: a warp per column, lanes over tiles;
+        // the per-rank columns are needed by tile 0 only
+        for (int c = warp; c < C; c += WARPS) {
+            if (tile != 0 && c >= E && c < E + R) continue;
+            const int32_t* col = counts + static_cast<size_t>(c) * T;
+            int32_t tot = 0, ex = 0;
+            for (int j = lane; j < T; j += 32) {
+                const int32_t v = ld_relaxed_s32(col + j);
+                tot += v;
+                ex += j < tile ? v : 0;
+            }
+            tot = __reduce_add_sync(FULL_MASK, tot);
+            ex = __reduce_add_sync(FULL_MASK, ex);
+            if (lane == 0) {
+                s_tot[c] = tot;
+                s_excl[c] = ex;
+            }
+        }
+        __syncthreads();
+        plan_totals<WARPS>(a, s_tot, s_pad, s_cu, s_warp, tile == 0);
+        for (int e = tid; e < E; e += THREADS) s_excl[e] += s_cu[e];  // first slot of e in this tile
+        __syncthreads();
+        tile_phase3<WARPS>(a, tile, s_excl, s_excl[E + R], s_excl[E + R + 1], s_wc, s_wg, s_wd, s_itr, s_items);
+        fill_unused<WARPS>(a, tile, T, s_cu, s_tot);
+    }
+
+    // ---- completion: the last CTA to finish closes the epoch
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        const uint32_t prev = atomicAdd(&a.hdr->done, 1u);
+        if (prev == gridDim.x - 1) {
+            a.hdr->ticket = 0u;
+            a.hdr->done = 0u;
+            a.hdr->epoch = epoch;
+            __threadfence();
+        }
+    }
 }
 
 }  // namespace moe
@@ -756,10 +1261,9 @@ constexpr int kMaxClusterTiles = 16;
 size_t cluster_smem(const Geom& g, int E, int R);
 
 // Tiles for the one-launch cluster path: as few iterations per warp as keep
-// the tile count within 16.  False when the plan needs more tiles, when the
-// tile's is_token_in_rank rows exceed 64 KB, or when MOE_PLAN_CLUSTER=0.
+// the tile count within 16.  False when the plan needs more tiles or when
+// the tile's is_token_in_rank rows exceed 64 KB.
 bool cluster_geometry(int N, int E, int K, int R, Geom* g) {
-    if (env_int("MOE_PLAN_CLUSTER", 1) == 0) return false;
     g->tpw = 32 / K;
     const int64_t per_tile_iter = static_cast<int64_t>(moe::PLAN_WARPS) * g->tpw;  // tokens
     const int64_t tiles1 = (static_cast<int64_t>(N) + per_tile_iter - 1) / per_tile_iter;
@@ -796,30 +1300,226 @@ cudaLaunchConfig_t cluster_config(int T, size_t smem, cudaStream_t stream, cudaL
     return cfg;
 }
 
-// Whether a cluster of T CTAs with this much shared memory fits the GPU
-// (cached per device, size and shared memory).
-bool cluster_launchable(int T, size_t smem) {
+// Whether a cluster of T CTAs of `kernel` with this much dynamic shared
+// memory fits the GPU (cached per device, kernel, size and shared memory).
+template <typename Kernel>
+bool cluster_launchable(Kernel kernel, int T, size_t smem) {
     static std::mutex mu;
-    static std::map<std::tuple<int, int, size_t>, bool> cache;
+    static std::map<std::tuple<int, const void*, int, size_t>, bool> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    const auto key = std::make_tuple(dev, T, smem);
+    const auto key = std::make_tuple(dev, reinterpret_cast<const void*>(kernel), T, smem);
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = cluster_config(T, smem, nullptr, attr, false);
     int n = 0;
-    const bool ok = cudaOccupancyMaxActiveClusters(&n, moe::plan_cluster_kernel, &cfg) == cudaSuccess && n >= 1;
+    const bool ok = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && n >= 1;
     if (!ok) cudaGetLastError();  // clear a sticky-free query error
     cache[key] = ok;
     return ok;
 }
 
-int launch_cluster(const PlanArgs& a, size_t smem, cudaStream_t stream) {
+template <typename Kernel>
+int launch_cluster(Kernel kernel, const PlanArgs& a, size_t smem, cudaStream_t stream) {
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = cluster_config(a.T, smem, stream, attr, moe_host::pdl_enabled());
-    return cudaLaunchKernelEx(&cfg, moe::plan_cluster_kernel, a) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, kernel, a) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// ---- small-E path geometry: 32 warps per CTA, the fewest warp steps
+// (1, 2, 4, 8) that keep the tiles within 16 (one cluster).
+bool small_geometry(int N, int E, int K, int R, Geom* g) {
+    if (E > moe::SMALL_MAX || R > moe::SMALL_MAX) return false;
+    g->tpw = 32 / K;
+    g->C = E + R + 2;
+    for (int ipt : {1, 2, 4, 8}) {
+        g->ipt = ipt;
+        g->tile_tokens = moe::PLAN_WARPS * ipt * g->tpw;
+        const int64_t T = (static_cast<int64_t>(N) + g->tile_tokens - 1) / g->tile_tokens;
+        if (T <= kMaxClusterTiles) {
+            g->T = static_cast<int>(T);
+            return true;
+        }
+    }
+    return false;
+}
+
+// NB = 3 when E <= 8 (so R <= 8), else 5.
+template <typename F>
+auto with_small_kernel(int ipt, int E, F&& f) {
+    if (E <= 8) {
+        switch (ipt) {
+            case 1: return f(moe::plan_small_kernel<1, 3>);
+            case 2: return f(moe::plan_small_kernel<2, 3>);
+            case 4: return f(moe::plan_small_kernel<4, 3>);
+            default: return f(moe::plan_small_kernel<8, 3>);
+        }
+    }
+    switch (ipt) {
+        case 1: return f(moe::plan_small_kernel<1, 5>);
+        case 2: return f(moe::plan_small_kernel<2, 5>);
+        case 4: return f(moe::plan_small_kernel<4, 5>);
+        default: return f(moe::plan_small_kernel<8, 5>);
+    }
+}
+
+// ---- grid path geometry: one warp iteration per tile with the fewest warps
+// (8, 16, 32) that keep the tiles within 152, else 32 warps and as many
+// iterations as needed (at most PLAN_IPT_MAX).  A function of the sizes
+// alone, like the workspace it implies; whether the tiles can all be
+// resident at once is checked per device at launch.
+constexpr int kGridMaxTiles = 152;
+
+size_t grid_smem(const Geom& g, int warps, int E, int R) {
+    const size_t ints = static_cast<size_t>(2 * warps * 32) * g.ipt + static_cast<size_t>(warps) * E +
+                        3 * static_cast<size_t>(g.C) + 2 * static_cast<size_t>(E + R + 2) + 4;  // + alignment
+    return sizeof(int32_t) * ints + (static_cast<size_t>(g.tile_tokens) * R + 15) / 16 * 16;
+}
+
+bool grid_geometry(int N, int E, int K, int R, Geom* g, int* warps) {
+    g->tpw = 32 / K;
+    int w = 0;
+    int64_t ipt = 1;
+    for (int cand : {8, 16, 32}) {
+        const int64_t tt = static_cast<int64_t>(cand) * g->tpw;
+        if ((static_cast<int64_t>(N) + tt - 1) / tt <= kGridMaxTiles) {
+            w = cand;
+            break;
+        }
+    }
+    if (w == 0) {
+        w = 32;
+        const int64_t per = static_cast<int64_t>(w) * g->tpw * kGridMaxTiles;
+        ipt = (static_cast<int64_t>(N) + per - 1) / per;
+        if (ipt > moe::PLAN_IPT_MAX) return false;
+    }
+    g->ipt = static_cast<int>(ipt);
+    g->tile_tokens = static_cast<int>(w * ipt * g->tpw);
+    g->T = static_cast<int>((static_cast<int64_t>(N) + g->tile_tokens - 1) / g->tile_tokens);
+    g->C = E + R + 2;
+    *warps = w;
+    if (static_cast<int64_t>(g->tile_tokens) * R > 65536) return false;
+    return g->T >= 1 && g->T <= kGridMaxTiles && grid_smem(*g, w, E, R) <= 220 * 1024;
+}
+
+// header, then flags u64[T], then counts i32[C][T]
+size_t grid_ws_bytes(const Geom& g) {
+    const size_t b = sizeof(moe::WsHeader) + sizeof(uint64_t) * static_cast<size_t>(g.T) +
+                     sizeof(int32_t) * static_cast<size_t>(g.T) * g.C;
+    return (b + 15) / 16 * 16;
+}
+
+// Workspace for every path the sizes allow.
+size_t plan_ws_bytes(int N, int E, int K, int R) {
+    size_t b = ws_bytes(plan_geometry(N, E, K, R));
+    Geom gg;
+    int w = 0;
+    if (grid_geometry(N, E, K, R, &gg, &w)) b = std::max(b, grid_ws_bytes(gg));
+    return b;
+}
+
+template <int W>
+int grid_occupancy(size_t smem) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, moe::plan_grid_kernel<W>, W * 32, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+// Whether all T CTAs can be resident at once (cached per device and shape).
+bool grid_launchable(int warps, int T, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, size_t>, bool> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const auto key = std::make_tuple(dev, warps, T, smem);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    const int per_sm = warps == 8 ? grid_occupancy<8>(smem) : warps == 16 ? grid_occupancy<16>(smem)
+                                                                          : grid_occupancy<32>(smem);
+    const bool ok = static_cast<int64_t>(per_sm) * moe_host::num_sms() >= T;
+    cache[key] = ok;
+    return ok;
+}
+
+int launch_grid(int warps, const PlanArgs& a, size_t smem, cudaStream_t stream) {
+    const dim3 grid(a.T), block(warps * 32);
+    if (warps == 8) return moe_host::launch(moe::plan_grid_kernel<8>, grid, block, smem, stream, a);
+    if (warps == 16) return moe_host::launch(moe::plan_grid_kernel<16>, grid, block, smem, stream, a);
+    return moe_host::launch(moe::plan_grid_kernel<32>, grid, block, smem, stream, a);
+}
+
+// Dynamic shared memory limits of every plan kernel, once per device.
+int ensure_kernel_attributes() {
+    static std::mutex mu;
+    static std::map<int, cudaError_t> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = done.find(dev);
+    if (it == done.end()) {
+        const int big = 220 * 1024;  // the geometries keep every plan kernel within this
+        const cudaError_t errs[] = {
+            cudaFuncSetAttribute(moe::plan_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, big),
+            cudaFuncSetAttribute(moe::plan_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, big),
+            cudaFuncSetAttribute(moe::plan_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, big),
+            cudaFuncSetAttribute(moe::plan_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_grid_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, big),
+            cudaFuncSetAttribute(moe::plan_grid_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, big),
+            cudaFuncSetAttribute(moe::plan_grid_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, big),
+            cudaFuncSetAttribute(moe::plan_small_kernel<1, 3>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<2, 3>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<4, 3>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<8, 3>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<1, 5>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<2, 5>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<4, 5>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<8, 5>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)};
+        cudaError_t first = cudaSuccess;
+        for (cudaError_t e : errs)
+            if (first == cudaSuccess) first = e;
+        it = done.emplace(dev, first).first;
+    }
+    return it->second == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Which path a plan of these sizes takes on the current device.  Default
+// order: the small-E cluster kernel, then the two-launch look-back plan.
+// MOE_PLAN_PATH=small|cluster|grid|lookback forces a path where the sizes
+// allow it (the look-back plan otherwise).
+enum PlanPath { PATH_SMALL = 0, PATH_CLUSTER = 1, PATH_GRID = 2, PATH_LOOKBACK = 3 };
+
+struct PathChoice {
+    int path;
+    Geom g;
+    int warps;
+    size_t smem;
+};
+
+PathChoice choose_path(int N, int E, int K, int R) {
+    const char* env = std::getenv("MOE_PLAN_PATH");
+    const std::string want = env != nullptr ? env : "auto";
+    const bool any = want == "auto";
+    Geom g;
+    int w = 0;
+    if ((any || want == "small") && small_geometry(N, E, K, R, &g)) {
+        const bool ok = with_small_kernel(g.ipt, E, [&](auto kern) { return cluster_launchable(kern, g.T, 0); });
+        if (ok) return PathChoice{PATH_SMALL, g, moe::PLAN_WARPS, 0};
+    }
+    if (want == "cluster" && cluster_geometry(N, E, K, R, &g)) {
+        const size_t smem = cluster_smem(g, E, R);
+        if (cluster_launchable(moe::plan_cluster_kernel, g.T, smem)) return PathChoice{PATH_CLUSTER, g, moe::PLAN_WARPS, smem};
+    }
+    if (want == "grid" && grid_geometry(N, E, K, R, &g, &w)) {
+        const size_t smem = grid_smem(g, w, E, R);
+        if (grid_launchable(w, g.T, smem)) return PathChoice{PATH_GRID, g, w, smem};
+    }
+    return PathChoice{PATH_LOOKBACK, plan_geometry(N, E, K, R), moe::PLAN_WARPS, 0};
 }
 
 }  // namespace
@@ -831,23 +1531,13 @@ extern "C" MOE_API int64_t moe_plan_capacity_rows(int N, int E, int K, int align
 
 extern "C" MOE_API size_t moe_plan_workspace_size(int N, int E, int K, int R) {
     if (check_sizes(N, E, K, R) != MOE_OK) return 0;
-    return ws_bytes(plan_geometry(N, E, K, R));
+    return plan_ws_bytes(N, E, K, R);
 }
 
 extern "C" MOE_API int moe_plan_launch_count(int N, int E, int K, int R) {
     if (check_sizes(N, E, K, R) != MOE_OK) return -1;
-    Geom cg;
-    if (cluster_geometry(N, E, K, R, &cg)) {
-        const int big = 200 * 1024;
-        if (cudaFuncSetAttribute(moe::plan_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, big) ==
-                cudaSuccess &&
-            cudaFuncSetAttribute(moe::plan_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-                cudaSuccess &&
-            cluster_launchable(cg.T, cluster_smem(cg, E, R)))
-            return 1;
-        cudaGetLastError();
-    }
-    return 2;
+    if (ensure_kernel_attributes() != MOE_OK) return -1;
+    return choose_path(N, E, K, R).path == PATH_LOOKBACK ? 2 : 1;
 }
 
 extern "C" MOE_API int moe_plan_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream) {
@@ -872,15 +1562,18 @@ extern "C" MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, in
         if (p == nullptr || !aligned(p, 4)) return MOE_ERR_INVALID_ARG;
     if (out->is_token_in_rank == nullptr || !aligned(workspace, 16)) return MOE_ERR_INVALID_ARG;
 
-    const Geom g = plan_geometry(N, E, K, R);
-    if (workspace_bytes < ws_bytes(g)) return MOE_ERR_CAPACITY;
+    if (workspace_bytes < plan_ws_bytes(N, E, K, R)) return MOE_ERR_CAPACITY;
+    rc = ensure_kernel_attributes();
+    if (rc != MOE_OK) return rc;
+    const PathChoice pc = choose_path(N, E, K, R);
+    const Geom& g = pc.g;
 
     PlanArgs a;
     a.topk = topk_idx;
     a.out = *out;
     a.hdr = static_cast<moe::WsHeader*>(workspace);
     a.flags = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) + sizeof(moe::WsHeader));
-    a.tile_prefix = reinterpret_cast<int32_t*>(a.flags + static_cast<size_t>(g.T) * g.C);
+    a.tile_prefix = reinterpret_cast<int32_t*>(a.flags + static_cast<size_t>(g.T) * (pc.path == PATH_GRID ? 1 : g.C));
     a.N = N;
     a.E = E;
     a.K = K;
@@ -897,30 +1590,13 @@ extern "C" MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, in
     a.skip_tile = moe_host::skip_tile();
     a.timeout_ns = moe_host::timeout_ns();
 
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        const int big = 220 * 1024;  // the geometry keeps every plan kernel within this
-        cudaError_t e1 = cudaFuncSetAttribute(moe::plan_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
-        cudaError_t e2 = cudaFuncSetAttribute(moe::plan_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
-        cudaError_t e3 = cudaFuncSetAttribute(moe::plan_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
-        cudaError_t e4 = cudaFuncSetAttribute(moe::plan_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        attr_err = e1 != cudaSuccess ? e1 : e2 != cudaSuccess ? e2 : e3 != cudaSuccess ? e3 : e4;
-    });
-    if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
-
-    // ---- one launch: a thread-block cluster of up to 16 tiles
-    Geom cg;
-    if (cluster_geometry(N, E, K, R, &cg)) {
-        PlanArgs c = a;
-        c.tpw = cg.tpw;
-        c.ipt = cg.ipt;
-        c.tile_tokens = cg.tile_tokens;
-        c.T = cg.T;
-        const size_t smem = cluster_smem(cg, E, R);
-        if (cluster_launchable(cg.T, smem)) return launch_cluster(c, smem, stream);
-    }
-
+    // ---- one launch: a thread-block cluster of up to 16 tiles, E, R <= 32
+    if (pc.path == PATH_SMALL)
+        return with_small_kernel(g.ipt, E, [&](auto kern) { return launch_cluster(kern, a, 0, stream); });
+    // ---- one launch: a thread-block cluster of up to 16 tiles, any E
+    if (pc.path == PATH_CLUSTER) return launch_cluster(moe::plan_cluster_kernel, a, pc.smem, stream);
+    // ---- one launch over the whole GPU, all tiles resident at once
+    if (pc.path == PATH_GRID) return launch_grid(pc.warps, a, pc.smem, stream);
     // ---- two launches: decoupled look-back over tiles, then the scatter
     const size_t smem1 = sizeof(int32_t) * (static_cast<size_t>(g.C) + 2 * (E + R + 2) + 2);
     const size_t smem2 = sizeof(int32_t) * (static_cast<size_t>(moe::PLAN_WARPS + 1) * E +
@@ -970,7 +1646,7 @@ extern "C" MOE_API int moe_plan_no_alloc(const int32_t* topk_idx, int N, int E, 
     int rc = check_sizes(N, E, K, R);
     if (rc != MOE_OK) return rc;
     if (alignment < 1) return MOE_ERR_INVALID_ARG;
-    const size_t need = ws_bytes(plan_geometry(N, E, K, R));
+    const size_t need = plan_ws_bytes(N, E, K, R);
     if (need > kNoAllocScratchBytes) return MOE_ERR_CAPACITY;
     void* ws = nullptr;
     rc = scratch_for_current_device(stream, &ws);

@@ -145,11 +145,13 @@ MOE_API size_t moe_plan_workspace_size(int N, int E, int K, int R);
 
 /*
  * Kernel launches moe_plan makes for these sizes on the current device: 1
- * when the plan fits one thread-block cluster of up to 16 tiles (one tile =
- * 16 warps x up to 8 steps x floor(32/K) tokens) and the GPU can co-schedule
- * it, else 2 (decoupled look-back, then the scatter).  -1 on bad sizes.
- * Setting the environment variable MOE_PLAN_CLUSTER=0 forces the 2-launch
- * path; both produce identical plans.
+ * when E <= 32, R <= 32 and the plan fits one thread-block cluster of up to
+ * 16 tiles (one tile = 32 warps x 1, 2, 4 or 8 steps x floor(32/K) tokens)
+ * that the GPU can co-schedule, else 2 (decoupled look-back, then the
+ * scatter).  -1 on bad sizes.  The environment variable
+ * MOE_PLAN_PATH=small|cluster|grid|lookback forces a path where the sizes
+ * allow it (cluster: a one-launch cluster plan for any E; grid: one launch
+ * of up to 152 co-resident tiles); every path produces the identical plan.
  */
 MOE_API int moe_plan_launch_count(int N, int E, int K, int R);
 

@@ -118,12 +118,13 @@ def plan_both(m, topk, E, R, a, out=None):
     return p, got, want
 
 
-@pytest.fixture(params=["auto", "lookback"])
+@pytest.fixture(params=["small", "cluster", "grid", "lookback"])
 def plan_path(request, monkeypatch):
-    """auto: one-launch cluster plan where the plan fits 16 tiles, else the
-    two-launch look-back plan; lookback: the look-back plan everywhere."""
-    if request.param == "lookback":
-        monkeypatch.setenv("MOE_PLAN_CLUSTER", "0")
+    """Force one plan path where the sizes allow it (the two-launch look-back
+    plan otherwise): small = the E, R <= 32 cluster kernel (the default where
+    it applies), cluster = the general cluster kernel, grid = one launch over
+    all SMs with every tile resident, lookback = the two-launch plan."""
+    monkeypatch.setenv("MOE_PLAN_PATH", request.param)
     return request.param
 
 
@@ -176,6 +177,15 @@ def test_plan_workspace_reuse_across_calls_and_sizes(m, plan_path):
         assert_plan_equal(got, want)
 
 
+def test_plan_launch_counts(m, monkeypatch):
+    assert m.plan_launches(16384, 8, 2, 4) == 1          # small-E cluster kernel
+    assert m.plan_launches(65536, 256, 8, 64) == 2       # look-back plan
+    monkeypatch.setenv("MOE_PLAN_PATH", "lookback")
+    assert m.plan_launches(16384, 8, 2, 4) == 2
+    monkeypatch.setenv("MOE_PLAN_PATH", "grid")
+    assert m.plan_launches(65536, 256, 8, 64) == 1
+
+
 def test_plan_bad_expert_id_reports_device_index(m):
     topk = np.zeros((64, 2), np.int32)
     topk[10, 1] = 8
@@ -183,8 +193,9 @@ def test_plan_bad_expert_id_reports_device_index(m):
     assert m.get_status(p) == 6
 
 
-def test_plan_uninitialised_workspace_reports_error(m, monkeypatch):
-    monkeypatch.setenv("MOE_PLAN_CLUSTER", "0")   # the look-back path is the one with a workspace
+@pytest.mark.parametrize("path", ["grid", "lookback"])     # the paths with a workspace
+def test_plan_uninitialised_workspace_reports_error(m, monkeypatch, path):
+    monkeypatch.setenv("MOE_PLAN_PATH", path)
     topk = workloads.random_topk(np.random.default_rng(3), 4000, 16, 4)
     t = torch.from_numpy(topk).to(dev())
     p = m.Plan.allocate(4000, 16, 4, 4, 8)
@@ -199,7 +210,9 @@ def test_plan_uninitialised_workspace_reports_error(m, monkeypatch):
     assert_plan_equal(p.to_host(), oracle.plan(topk, 16, 4, 8))
 
 
-def test_plan_bounded_wait_reports_timeout_and_recovers(m):
+@pytest.mark.parametrize("path", ["grid", "lookback"])     # the paths that wait on other tiles
+def test_plan_bounded_wait_reports_timeout_and_recovers(m, monkeypatch, path):
+    monkeypatch.setenv("MOE_PLAN_PATH", path)
     N, E, K, R, a = 20000, 64, 8, 8, 16     # several tiles
     topk = workloads.random_topk(np.random.default_rng(4), N, E, K)
     t = torch.from_numpy(topk).to(dev())
