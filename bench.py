@@ -268,7 +268,7 @@ def run_ours(args, w):
         m.plan(idx, w.E, w.R, w.alignment, out=p)
         if ev:
             ev[2].record(stream)
-        m.permute(x, p, out=perm)
+        m.permute(x, p, out=perm, early_x=True)
         if ev:
             ev[3].record(stream)
         m.combine(perm, wts, p, out=out)
@@ -284,20 +284,29 @@ def run_ours(args, w):
         raise RuntimeError("device status %d during warm-up" % status)
     P = int(p.cu_seqlens[-1].item())
 
-    # ---- one step (and each stage alone) captured as CUDA graphs: the
-    # timed region replays them, so host-side launch cost is not measured
+    # ---- one step, and each stage alone (10 back-to-back calls, so that a
+    # graph launch does not bound a µs-scale kernel), captured as CUDA
+    # graphs: the timed region replays them, so host-side launch cost is not
+    # measured
+    stage_reps = 10
+    # the timed steps run as graphs of up to 10 steps (as a model captures
+    # many MoE layers in one graph) plus one graph per leftover step
+    steps_per_graph = 10
     graph_stream = torch.cuda.Stream()
     graph_stream.wait_stream(stream)
     graphs = {}
     with torch.cuda.stream(graph_stream):
-        for name, fn in (("step", step), ("route", lambda: m.route_topk(logits, w.K, topk_idx=idx, topk_w=wts, **rk)),
-                         ("plan", lambda: m.plan(idx, w.E, w.R, w.alignment, out=p)),
-                         ("permute", lambda: m.permute(x, p, out=perm)),
-                         ("combine", lambda: m.combine(perm, wts, p, out=out))):
+        for name, fn, reps in (("step", step, 1), ("chunk", step, steps_per_graph),
+                               ("route", lambda: m.route_topk(logits, w.K, topk_idx=idx, topk_w=wts, **rk), stage_reps),
+                               ("plan", lambda: m.plan(idx, w.E, w.R, w.alignment, out=p), stage_reps),
+                               # standalone: no overlap with the previous call's tail
+                               ("permute", lambda: m.permute(x, p, out=perm), stage_reps),
+                               ("combine", lambda: m.combine(perm, wts, p, out=out), stage_reps)):
             fn()  # warm on the capture stream
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=graph_stream):
-                fn()
+                for _ in range(reps):
+                    fn()
             graphs[name] = g
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
@@ -312,50 +321,91 @@ def run_ours(args, w):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1)
 
+    def timed_steps(k):
+        """Exactly k steps: k // 10 replays of the 10-step graph, k % 10 of the 1-step one."""
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k // steps_per_graph):
+            graphs["chunk"].replay()
+        for _ in range(k % steps_per_graph):
+            graphs["step"].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
     for _ in range(max(3, args.warmup)):
         graphs["step"].replay()
+    graphs["chunk"].replay()
     torch.cuda.synchronize()
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[torch.cuda.current_device()]))
     with clocks:
         barrier()
         torch.cuda.synchronize()
-        local_ms = timed(graphs["step"], args.steps)  # the timed region: K steps
+        local_ms = timed_steps(args.steps)  # the timed region: K steps
         barrier()
         # each kernel alone, same inputs, for its achieved bandwidth
-        stage_ms = {k: timed(graphs[k], args.steps) / args.steps for k in ("route", "plan", "permute", "combine")}
+        stage_ms = {k: timed(graphs[k], args.steps) / (args.steps * stage_reps)
+                    for k in ("route", "plan", "permute", "combine")}
     ms = reduce_max(local_ms)
     assert m.get_status(p) == 0
 
-    # ---- end to end through host buffers (pinned), copies inside the region
-    h_logits = torch.from_numpy(inp["logits"]).pin_memory()
-    h_x = torch.from_numpy(inp["x_bits"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_out = torch.empty((w.N, w.H), dtype=torch.bfloat16).pin_memory()
-    d_logits = torch.empty_like(logits)
-    d_x = torch.empty_like(x)
+    # ---- end to end through host buffers (pinned), copies inside the
+    # region: a two-deep pipeline as a serving loop runs it -- step i's
+    # host->device copies (copy stream) overlap step i-1's kernels (compute
+    # stream) and step i-2's device->host copy (second copy stream); inputs
+    # and outputs are double-buffered on both sides, and every step copies
+    # its own inputs in and its own result out
+    h_logits = [torch.from_numpy(inp["logits"]).pin_memory() for _ in range(2)]
+    h_x = [torch.from_numpy(inp["x_bits"].view(np.int16)).view(torch.bfloat16).pin_memory() for _ in range(2)]
+    h_out = [torch.empty((w.N, w.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    d_logits = [torch.empty_like(logits) for _ in range(2)]
+    d_x = [torch.empty_like(x) for _ in range(2)]
+    d_out = [torch.empty_like(out) for _ in range(2)]
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "used", "done", "out")}
 
-    def e2e_step():
-        d_logits.copy_(h_logits, non_blocking=True)
-        d_x.copy_(h_x, non_blocking=True)
-        m.route_topk(d_logits, w.K, topk_idx=idx, topk_w=wts, **rk)
-        m.plan(idx, w.E, w.R, w.alignment, out=p)
-        m.permute(d_x, p, out=perm)
-        m.combine(perm, wts, p, out=out)
-        h_out.copy_(out, non_blocking=True)
+    def e2e_step(i):
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev["used"][b])        # step i-2 has consumed buffer b
+            d_logits[b].copy_(h_logits[b], non_blocking=True)
+            d_x[b].copy_(h_x[b], non_blocking=True)
+            ev["in"][b].record(s_in)
+        with torch.cuda.stream(s_cmp):
+            s_cmp.wait_event(ev["in"][b])
+            if i >= 2:
+                s_cmp.wait_event(ev["out"][b])       # step i-2's result has left d_out[b]
+            m.route_topk(d_logits[b], w.K, topk_idx=idx, topk_w=wts, **rk)
+            m.plan(idx, w.E, w.R, w.alignment, out=p)
+            m.permute(d_x[b], p, out=perm, early_x=True)
+            ev["used"][b].record(s_cmp)
+            m.combine(perm, wts, p, out=d_out[b])
+            ev["done"][b].record(s_cmp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["done"][b])
+            h_out[b].copy_(d_out[b], non_blocking=True)
+            ev["out"][b].record(s_out)
 
-    for _ in range(2):
-        e2e_step()
+    for i in range(4):
+        e2e_step(i)
     torch.cuda.synchronize()
-    e_steps = max(3, args.steps // 2)
+    e_steps = max(6, args.steps)
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_in)
+    s_cmp.wait_event(e0)
+    s_out.wait_event(e0)
+    for i in range(e_steps):
+        e2e_step(i)
+    e1.record(s_out)          # s_out's last copy ends the region (it waits on every earlier stage)
     torch.cuda.synchronize()
     e2e_ms = reduce_max(e0.elapsed_time(e1)) / e_steps
+    if m.get_status(p) != 0:
+        raise RuntimeError("device status during the end-to-end run")
     barrier()
 
     if rank != 0:
@@ -381,7 +431,8 @@ def run_ours(args, w):
         "config": config_of(w, extra={"P": P, "l2": "inputs larger than L2 (%.0f MB touched per step)"
                                       % (sum(ab[k] for k in ("permute", "combine")) / 1e6),
                                       "experts": "identity (combine reads the permuted rows)",
-                                      "launch": "CUDA graph of one step, replayed K times"}),
+                                      "launch": "CUDA graphs of 10 steps (and of 1 step for K mod 10)",
+                                      "permute": "early_x: x row loads overlap the plan kernel"}),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "traffic": committed_traffic(dom, w.name),
@@ -390,8 +441,9 @@ def run_ours(args, w):
         "route_plan_us": round(1e3 * (stage_ms["route"] + stage_ms["plan"]), 2),
         "cpu_baseline": cpu,
         "e2e": {"value": ws * w.N / (e2e_ms * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": int(h_logits.numel() * 4 + h_x.numel() * 2),
-                "d2h_bytes_per_step": int(h_out.numel() * 2), "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": int(h_logits[0].numel() * 4 + h_x[0].numel() * 2),
+                "d2h_bytes_per_step": int(h_out[0].numel() * 2), "ms_per_step": e2e_ms,
+                "method": "two-deep pipeline: H2D, kernels and D2H on three streams, double-buffered"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }

@@ -57,7 +57,7 @@ SIGNATURES = [
                                  _i32, ctypes.c_int32, ctypes.POINTER(MoeBalancedPlanOut), _P]),
     ("moe_tile_map", _i32, [ctypes.POINTER(MoePlanOut), _i32, _i32, _P, _P, _i64, _P, _P]),
     ("moe_rank_layout", _i32, [ctypes.POINTER(MoePlanOut), _i32, _i32, _i32, _P, _P, _P]),
-    ("moe_permute", _i32, [_P, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(MoePlanOut), _P, _P]),
+    ("moe_permute", _i32, [_P, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(MoePlanOut), _P, _i32, _P]),
     ("moe_combine", _i32, [_P, _P, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(MoePlanOut), _P, _P]),
     ("moe_get_status", _i32, [ctypes.POINTER(MoePlanOut), ctypes.POINTER(ctypes.c_int32), _P]),
     ("moe_debug_set_plan_fault", _i32, [_i32, _i64]),
@@ -65,6 +65,9 @@ SIGNATURES = [
 
 _lock = threading.Lock()
 _lib = None
+
+
+MOE_PERMUTE_EARLY_X = 1  # moe_permute flag (include/moe_dispatch.h)
 
 
 class MoeError(RuntimeError):

@@ -11,7 +11,7 @@ from dataclasses import dataclass, field
 import torch
 
 from . import _lib
-from ._lib import MoeBalancedPlanOut, MoePlanOut, check, load
+from ._lib import MOE_PERMUTE_EARLY_X, MoeBalancedPlanOut, MoePlanOut, check, load
 
 SCORING = {"softmax": _lib.MOE_SCORING_SOFTMAX, "sigmoid": _lib.MOE_SCORING_SIGMOID,
            0: 0, 1: 1}
@@ -228,15 +228,21 @@ def rank_layout(p: Plan, num_channels: int, stream=None):
     return cpm, trs
 
 
-def permute(x: torch.Tensor, p: Plan, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Expert-contiguous copy of x bf16[N,H] -> bf16[P_cap,H] (rows >= P untouched)."""
+def permute(x: torch.Tensor, p: Plan, out: torch.Tensor | None = None, stream=None,
+            early_x: bool = False) -> torch.Tensor:
+    """Expert-contiguous copy of x bf16[N,H] -> bf16[P_cap,H] (rows >= P untouched).
+
+    early_x: start loading x before the previous kernel on the stream ends
+    (MOE_PERMUTE_EARLY_X); only when that kernel does not write x, e.g.
+    directly after the plan() call that built p, with x produced before it.
+    """
     N, H = x.shape
     _need(x, torch.bfloat16, (p.N, H), "x")
     if out is None:
         out = torch.empty((p.P_cap, H), dtype=torch.bfloat16, device=x.device)
     _need(out, torch.bfloat16, (p.P_cap, H), "permuted")
     rc = load().moe_permute(_ptr(x), N, H, p.K, p.E, p.alignment, ctypes.byref(p.c_struct), _ptr(out),
-                            _stream(stream))
+                            MOE_PERMUTE_EARLY_X if early_x else 0, _stream(stream))
     check("moe_permute", rc)
     return out
 

@@ -705,8 +705,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_cluster_kernel(const PlanAr
 // same-expert pairs and the (token, rank) duplicate test, and the token's
 // rank bitmask is written straight to is_token_in_rank.  One CTA barrier
 // turns the per-warp counts into warp bases (lanes split over experts and
-// warps, xor-shuffle sums); each CTA then pushes its tile's counts into the
-// shared memory of every CTA of the cluster (remote stores, no round trip),
+// warps, xor-shuffle sums); warp q of each CTA then pushes its tile's counts
+// into the shared memory of CTA q of the cluster (remote stores, no round trip),
 // and after one cluster barrier every warp derives the tile prefixes, the
 // totals and cu_seqlens from its own shared memory and writes its pairs'
 // slots.  Tile 0's warp 0 writes the totals-derived outputs.  Per-pair
@@ -747,7 +747,6 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs
     __shared__ int32_t s_wc[PLAN_WARPS][EP + 1];  // per-warp pairs per expert (+1: no bank conflicts)
     __shared__ int32_t s_wr[PLAN_WARPS][EP + 1];  // per-warp tokens per rank
     __shared__ int32_t s_wg[PLAN_WARPS], s_wd[PLAN_WARPS];
-    __shared__ int32_t s_cnt[CW];                 // this tile's counts
     __shared__ int32_t s_all[16][CW];             // every tile's counts, pushed by its CTA
 
     pdl_wait();
@@ -820,11 +819,14 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs
         // duplicates of a token: group after group (groups in order of their
         // primary lane), k order inside a group; a warp scan of the group
         // sizes gives the duplicates of the groups opening before a lane
-        const int my_p = __ffs(pd) - 1;
-        const int gsz = opens ? __popc(pd) - 1 : 0;
-        const int excl = warp_incl_scan(gsz, 32) - gsz;
-        const int tok_base = __shfl_sync(FULL_MASK, excl, tok_lane0 & 31);
-        const int groups_before = __shfl_sync(FULL_MASK, excl, my_p & 31) - tok_base;
+        int groups_before = 0;  // with K <= 2 a token has at most one group
+        if (K > 2) {
+            const int my_p = __ffs(pd) - 1;
+            const int gsz = opens ? __popc(pd) - 1 : 0;
+            const int excl = warp_incl_scan(gsz, 32) - gsz;
+            const int tok_base = __shfl_sync(FULL_MASK, excl, tok_lane0 & 31);
+            groups_before = __shfl_sync(FULL_MASK, excl, my_p & 31) - tok_base;
+        }
         const int before = groups_before + (dup ? __popc(pd & lt) - 1 : 0);
         const int dup_pos = run_d + __popc(dball & below_tok) + before;
 
@@ -879,8 +881,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs
     const int g_wbase = __reduce_add_sync(FULL_MASK, lane < warp ? vg : 0);
     const int d_wbase = __reduce_add_sync(FULL_MASK, lane < warp ? vd : 0);
 
-    // ---- warp 0: the tile's counts, pushed into every CTA's s_all[tile]
-    if (warp == 0) {
+    // ---- the tile's counts; warp q pushes them into CTA q's s_all[tile]
+    if (static_cast<uint32_t>(warp) < ncta) {
         int tile_r = 0;
         {
             int v[EP];
@@ -892,18 +894,13 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs
             for (int off = EP; off < 32; off <<= 1) tile_r += __shfl_xor_sync(FULL_MASK, tile_r, off);
         }
         const int g_tile = __reduce_add_sync(FULL_MASK, vg), d_tile = __reduce_add_sync(FULL_MASK, vd);
-        if (lane < EP) {
-            s_cnt[lane] = tile_e;
-            s_cnt[EP + lane] = tile_r;
-        }
-        if (lane == 0) {
-            s_cnt[2 * EP] = g_tile;
-            s_cnt[2 * EP + 1] = d_tile;
-        }
-        __syncwarp();
-        for (int idx = lane; idx < static_cast<int>(ncta) * CW; idx += 32) {
-            const int q = idx / CW, c = idx - q * CW;
-            st_dsmem_s32(dsmem_addr(&s_all[tile][c], static_cast<uint32_t>(q)), s_cnt[c]);
+#pragma unroll
+        for (int c0 = 0; c0 < CW; c0 += 32) {
+            const int c = c0 + lane;
+            const int ve = __shfl_sync(FULL_MASK, tile_e, c & (EP - 1));
+            const int vr = __shfl_sync(FULL_MASK, tile_r, (c - EP) & (EP - 1));
+            const int val = c < EP ? ve : c < 2 * EP ? vr : c == 2 * EP ? g_tile : d_tile;
+            if (c < CW) st_dsmem_s32(dsmem_addr(&s_all[tile][c], static_cast<uint32_t>(warp)), val);
         }
     }
     cluster_arrive();  // release: this CTA's pushes

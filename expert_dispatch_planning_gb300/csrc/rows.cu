@@ -37,6 +37,7 @@ struct PermuteArgs {
     uint32_t stage_bytes;  // G * row bytes rounded up to 128
     uint32_t slots_bytes;  // stages * G * K * 4 rounded up to 128
     int64_t timeout_ns;
+    int early_x;  // load the first stages' x rows before waiting on the predecessor kernel
 };
 
 __global__ void __launch_bounds__(32) permute_kernel(const PermuteArgs a) {
@@ -44,10 +45,6 @@ __global__ void __launch_bounds__(32) permute_kernel(const PermuteArgs a) {
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);                  // [stages]
     int32_t* slots = reinterpret_cast<int32_t*>(smem + 128);             // [stages][G*K]
     uint8_t* rows = smem + 128 + a.slots_bytes;                          // [stages][stage_bytes]
-
-    pdl_wait();
-    pdl_trigger();
-    if (ld_volatile_s32(a.status) != 0) return;  // no valid plan to move rows by
 
     const int lane = threadIdx.x;
     const int K = a.K, G = a.G;
@@ -63,7 +60,20 @@ __global__ void __launch_bounds__(32) permute_kernel(const PermuteArgs a) {
     const int64_t g_end = (blockIdx.x + 1) * a.n_groups / gridDim.x;
     const int64_t n_mine = g_end - g_begin;
 
-    auto issue = [&](int64_t i) {  // load group g_begin + i into stage i % stages
+    // A stage completes when its x rows (one bulk load, lane 0's arrive with
+    // the byte count) and its dst entries (4-byte cp.async loads, one
+    // no-increment arrive per lane) have landed: 33 arrivals.
+    auto issue_x = [&](int64_t i) {  // x rows of group g_begin + i into stage i % stages
+        if (lane == 0) {
+            const int st = static_cast<int>(i % a.stages);
+            const int64_t tok0 = (g_begin + i) * G;
+            const int ntok = static_cast<int>(min(static_cast<int64_t>(G), static_cast<int64_t>(a.N) - tok0));
+            const uint32_t bytes = static_cast<uint32_t>(ntok) * row_bytes;
+            mbar_arrive_expect_tx(&bar[st], bytes);
+            bulk_g2s(rows + static_cast<size_t>(st) * a.stage_bytes, a.x + tok0 * H, bytes, &bar[st]);
+        }
+    };
+    auto issue_dst = [&](int64_t i) {  // the group's dst entries
         const int st = static_cast<int>(i % a.stages);
         const int64_t tok0 = (g_begin + i) * G;
         const int ntok = static_cast<int>(min(static_cast<int64_t>(G), static_cast<int64_t>(a.N) - tok0));
@@ -71,14 +81,28 @@ __global__ void __launch_bounds__(32) permute_kernel(const PermuteArgs a) {
         int32_t* sl = slots + st * G * K;
         for (int p = lane; p < npairs; p += 32) cp_async_4(sl + p, a.dst + tok0 * K + p);
         cp_async_mbar_arrive_noinc(&bar[st]);
-        if (lane == 0) {
-            const uint32_t bytes = static_cast<uint32_t>(ntok) * row_bytes;
-            mbar_arrive_expect_tx(&bar[st], bytes);
-            bulk_g2s(rows + static_cast<size_t>(st) * a.stage_bytes, a.x + tok0 * H, bytes, &bar[st]);
-        }
+    };
+    auto issue = [&](int64_t i) {
+        issue_dst(i);
+        issue_x(i);
     };
 
+    // x does not depend on the plan: with early_x the first stages' rows
+    // are requested while the previous kernel (normally the plan) still runs
     int64_t issued = 0;
+    if (a.early_x)
+        for (; issued < a.stages && issued < n_mine; ++issued) issue_x(issued);
+
+    pdl_wait();
+    pdl_trigger();
+    if (ld_volatile_s32(a.status) != 0) {  // no valid plan to move rows by
+        // complete the prefetched stages and let their rows land before the
+        // CTA releases its shared memory
+        for (int64_t j = 0; j < issued; ++j) cp_async_mbar_arrive_noinc(&bar[j]);
+        for (int64_t j = 0; j < issued; ++j) mbar_wait_bounded(&bar[j], 0u, static_cast<uint64_t>(a.timeout_ns));
+        return;
+    }
+    for (int64_t j = 0; j < issued; ++j) issue_dst(j);
     for (; issued < a.stages && issued < n_mine; ++issued) issue(issued);
 
     bool failed = false;
@@ -284,10 +308,11 @@ constexpr size_t kSmemPerSm = 227 * 1024;
 }  // namespace
 
 extern "C" MOE_API int moe_permute(const uint16_t* x, int N, int H, int K, int E, int alignment,
-                                   const MoePlanOut* plan, uint16_t* permuted, cudaStream_t stream) {
+                                   const MoePlanOut* plan, uint16_t* permuted, int flags, cudaStream_t stream) {
     if (x == nullptr || plan == nullptr || permuted == nullptr || plan->dst == nullptr ||
         plan->zero_fill_ranges == nullptr || plan->status == nullptr)
         return MOE_ERR_INVALID_ARG;
+    if ((flags & ~MOE_PERMUTE_EARLY_X) != 0) return MOE_ERR_INVALID_ARG;
     if (N < 1 || K < 1 || K > 32 || E < 1 || E > 1024 || K > E || alignment < 1 || H < 8 || H % 8 != 0)
         return MOE_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(permuted, 16) || !aligned(plan->dst, 4)) return MOE_ERR_INVALID_ARG;
@@ -334,6 +359,7 @@ extern "C" MOE_API int moe_permute(const uint16_t* x, int N, int H, int K, int E
     a.slots_bytes = slots_for(stages);
     a.n_groups = (N + G - 1) / G;
     a.timeout_ns = moe_host::timeout_ns();
+    a.early_x = (flags & MOE_PERMUTE_EARLY_X) != 0 ? 1 : 0;
     if (128 + a.slots_bytes + static_cast<size_t>(stages) * a.stage_bytes > kSmemPerSm) return MOE_ERR_UNSUPPORTED;
     int per_sm = env_int("MOE_PERMUTE_CTAS_PER_SM", 6);
     if (per_sm < 1) per_sm = 1;

@@ -291,6 +291,9 @@ MOE_API int moe_rank_layout(const MoePlanOut* plan, int N, int R, int num_channe
                             int32_t* channel_prefix_matrix, int32_t* token_rank_slot, cudaStream_t stream);
 
 /* ---------------------------------------------------------------- rows */
+/* moe_permute flags. */
+#define MOE_PERMUTE_EARLY_X 1  /* see moe_permute */
+
 /*
  * Permute (DeepEP dispatch's hidden-row copy, MoonEP dst / zero_fill_ranges):
  *   permuted[raw slot(f)] = x[f / K] for every pair, primaries and
@@ -300,9 +303,18 @@ MOE_API int moe_rank_layout(const MoePlanOut* plan, int N, int R, int num_channe
  *   permuted  (device) bf16[P_cap][H], 16-byte aligned, must not alias x.
  *   plan      the plan built by moe_plan for the same N, E, K, alignment
  *             (uses dst, zero_fill_ranges, status).
+ *   flags     0, or MOE_PERMUTE_EARLY_X: the kernel starts loading x rows
+ *             before the kernel enqueued just before it on `stream` has
+ *             finished (it waits for that kernel before reading the plan).
+ *             Allowed only when that kernel does not write x -- as when
+ *             moe_permute directly follows the moe_plan call that built
+ *             `plan` and x was produced before it; never when x comes from
+ *             the kernel right before (a plan reused for new hidden states).
+ * If the plan's status holds an error the call writes nothing.  Other
+ * flag bits: MOE_ERR_INVALID_ARG.
  */
 MOE_API int moe_permute(const uint16_t* x, int N, int H, int K, int E, int alignment,
-                        const MoePlanOut* plan, uint16_t* permuted, cudaStream_t stream);
+                        const MoePlanOut* plan, uint16_t* permuted, int flags, cudaStream_t stream);
 
 /*
  * Weighted combine (DeepEP combine's fp32 accumulation and bf16 store):

@@ -116,9 +116,10 @@ def test_plan_rejects_bad_arguments(lib):
 
 def test_rows_reject_bad_arguments(lib):
     out = _plan_struct()
-    assert lib.moe_permute(FAKE, 4, 12, 2, 8, 2, ctypes.byref(out), FAKE, None) == 1     # H % 8
-    assert lib.moe_permute(P(0x10008), 4, 16, 2, 8, 2, ctypes.byref(out), FAKE, None) == 1
-    assert lib.moe_permute(FAKE, 4, 65536, 2, 8, 2, ctypes.byref(out), FAKE, None) == 2  # row > 96 KB
+    assert lib.moe_permute(FAKE, 4, 12, 2, 8, 2, ctypes.byref(out), FAKE, 0, None) == 1     # H % 8
+    assert lib.moe_permute(P(0x10008), 4, 16, 2, 8, 2, ctypes.byref(out), FAKE, 0, None) == 1
+    assert lib.moe_permute(FAKE, 4, 65536, 2, 8, 2, ctypes.byref(out), FAKE, 0, None) == 2  # row > 96 KB
+    assert lib.moe_permute(FAKE, 4, 16, 2, 8, 2, ctypes.byref(out), FAKE, 2, None) == 1     # unknown flag
     assert lib.moe_combine(FAKE, FAKE, 4, 2, 12, 8, 2, ctypes.byref(out), FAKE, None) == 1
     assert lib.moe_combine(FAKE, FAKE, 4, 9, 16, 8, 2, ctypes.byref(out), FAKE, None) == 1  # K > E
     assert lib.moe_combine(FAKE, FAKE, 4, 2, 16, 8, 2, None, FAKE, None) == 1

@@ -268,6 +268,42 @@ def test_permute_combine_configs(m, name):
     assert m.get_status(p) == 0
 
 
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "qwen3", "dsv3"])
+def test_permute_early_x_right_after_plan(m, name):
+    """MOE_PERMUTE_EARLY_X directly after the plan call, x produced before it:
+    the rows loaded while the plan kernel still runs give the same buffer."""
+    w = workloads.get(name)
+    inp = workloads.make_inputs(w, seed=0)
+    o_idx, _ = oracle.route_topk(inp["logits"], w.K, bias=inp["bias"], **route_kwargs(w))
+    want = oracle.plan(o_idx, w.E, w.R, w.alignment)
+    x = to_bf16(inp["x_bits"])
+    idx = torch.from_numpy(o_idx).to(dev())
+    p = m.Plan.allocate(w.N, w.E, w.K, w.R, w.alignment)
+    perm = torch.full((p.P_cap, w.H), -3.0, dtype=torch.bfloat16, device=dev())
+    for _ in range(2):                      # back to back, no synchronisation in between
+        m.plan(idx, w.E, w.R, w.alignment, out=p)
+        m.permute(x, p, out=perm, early_x=True)
+    o_perm = oracle.permute(inp["x_bits"], want["dst"], want["zero_fill_ranges"], w.K, want["P_cap"],
+                            fill=np.full((want["P_cap"], w.H), bits(torch.tensor([-3.0], dtype=torch.bfloat16))[0],
+                                         np.uint16))
+    assert np.array_equal(bits(perm), o_perm)
+    assert m.get_status(p) == 0
+
+
+def test_permute_early_x_after_failed_plan_writes_nothing(m):
+    topk = workloads.random_topk(np.random.default_rng(5), 4096, 8, 2)
+    topk[100, 1] = 8                                             # expert id out of range
+    x = torch.ones((4096, 256), dtype=torch.bfloat16, device=dev())
+    idx = torch.from_numpy(topk).to(dev())
+    p = m.Plan.allocate(4096, 8, 2, 4, 16)
+    sentinel = torch.full((p.P_cap, 256), 7.0, dtype=torch.bfloat16, device=dev())
+    m.plan(idx, 8, 4, 16, out=p)
+    m.permute(x, p, out=sentinel, early_x=True)
+    torch.cuda.synchronize()
+    assert m.get_status(p) == 6
+    assert bool((sentinel == 7.0).all())
+
+
 def test_permute_combine_large_sampled(m):
     """Full-size large config in the benchmark's launch configuration; rows
     checked by properties on the device and sampled tokens against the oracle."""
@@ -275,7 +311,7 @@ def test_permute_combine_large_sampled(m):
     x = to_bf16(inp["x_bits"])
     perm = torch.empty((p.P_cap, w.H), dtype=torch.bfloat16, device=dev())
     perm[want["P"]:] = 5.0
-    m.permute(x, p, out=perm)
+    m.permute(x, p, out=perm, early_x=True)     # as the benchmark launches it (the fill above is not x)
     # every pair's row equals its token row (checked on the device, in chunks)
     raw = np.where(want["dst"] >= 0, want["dst"], -want["dst"] - 1).astype(np.int64)
     raw_t = torch.from_numpy(raw).to(dev())
