@@ -18,6 +18,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import subprocess
 import sys
 import time
@@ -183,6 +184,21 @@ def oracle_sample_tokens(w) -> int:
     return min(w.N, max(256, int(2.0e8 // (w.K * w.H + 1))))
 
 
+def host_cpu():
+    """nproc and the CPU model of this host (for the oracle's timing)."""
+    model = platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                if k.strip().lower() in ("model name", "cpu part") and v.strip():
+                    model = "%s (%s %s)" % (platform.machine(), k.strip(), v.strip())
+                    break
+    except OSError:
+        pass
+    return {"nproc": os.cpu_count(), "cpu": model}
+
+
 def cpu_baseline(w, inp, min_seconds=10.0, max_steps=40):
     n = oracle_sample_tokens(w)
     oracle_step(w, inp, n)   # warm (builds/loads the library)
@@ -195,7 +211,7 @@ def cpu_baseline(w, inp, min_seconds=10.0, max_steps=40):
     return {"value": n * steps / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": "%d full oracle steps (route+plan+permute+combine) on the first %d of %d tokens "
                       "of the %s workload, single-threaded C" % (steps, n, w.N, w.name),
-            "seconds": round(dt, 2)}
+            "seconds": round(dt, 2), "host": host_cpu()}
 
 
 def run_reference(args, w):
@@ -217,7 +233,8 @@ def run_reference(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config_of(w, extra={"sample_tokens": n}),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": "first %d of %d tokens per step, single-threaded C oracle" % (n, w.N)},
+                         "sample": "first %d of %d tokens per step, single-threaded C oracle" % (n, w.N),
+                         "host": host_cpu()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -321,8 +338,25 @@ def run_ours(args, w):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1)
 
+    # inputs smaller than twice the 129 MB L2: flush it (a 256 MB memset)
+    # before every timed step and time the steps one by one
+    touched = sum(algorithmic_bytes(w, P)[k] for k in ("route", "permute", "combine"))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if touched < 2 * L2_BYTES else None
+
     def timed_steps(k):
         """Exactly k steps: k // 10 replays of the 10-step graph, k % 10 of the 1-step one."""
+        if flush is not None:
+            total = 0.0
+            for _ in range(k):
+                flush.zero_()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graphs["step"].replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                total += e0.elapsed_time(e1)
+            return total
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -428,10 +462,13 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_of(w, extra={"P": P, "l2": "inputs larger than L2 (%.0f MB touched per step)"
-                                      % (sum(ab[k] for k in ("permute", "combine")) / 1e6),
+        "config": config_of(w, extra={"P": P, "l2": ("inputs larger than L2 (%.0f MB touched per step)"
+                                                     % (touched / 1e6)) if flush is None else
+                                      ("L2 flushed (256 MB memset) before each timed step, steps timed one by one; "
+                                       "%.1f MB touched per step" % (touched / 1e6)),
                                       "experts": "identity (combine reads the permuted rows)",
-                                      "launch": "CUDA graphs of 10 steps (and of 1 step for K mod 10)",
+                                      "launch": "CUDA graphs of 10 steps (and of 1 step for K mod 10)"
+                                      if flush is None else "CUDA graph of one step per timed step",
                                       "permute": "early_x: x row loads overlap the plan kernel"}),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_kind,

@@ -1,6 +1,13 @@
 // plan.cu -- dispatch plan for one GPU (sm_103a): histogram, aligned
 // offsets, stable slots, per-rank duplicate detection, rank matrices and
-// the dedup structures, in two launches and without any grid barrier.
+// the dedup structures.  Four paths compute the identical plan:
+//   - plan_small_kernel (default for E <= 32, R <= 32): one cluster launch,
+//     lanes own experts and ranks, counts pushed between CTAs (described
+//     at the kernel);
+//   - plan_count_kernel + plan_scatter_kernel (default otherwise): two
+//     launches with a decoupled look-back, described below;
+//   - plan_cluster_kernel and plan_grid_kernel: one launch for any E, on
+//     request (MOE_PLAN_PATH), described at the kernels.
 //
 // Pairs are cut into tiles of whole tokens.  Inside a tile each warp owns a
 // contiguous run of tokens and walks it in iterations of floor(32/K) tokens,
