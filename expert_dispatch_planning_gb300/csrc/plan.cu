@@ -756,8 +756,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs
     __shared__ int32_t s_wg[PLAN_WARPS], s_wd[PLAN_WARPS];
     __shared__ int32_t s_all[16][CW];             // every tile's counts, pushed by its CTA
 
-    pdl_wait();
-    pdl_trigger();
+    // set-up that reads no memory of the previous kernels runs before the wait
     cluster_arrive_relaxed();  // this CTA has started: the others may push into it once all have
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int E = a.E, K = a.K, R = a.R;
@@ -775,6 +774,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs
 #pragma unroll
     for (int b = 0; b < NB; ++b) xl[b] = 0u - ((static_cast<unsigned>(lane) >> b) & 1u);
 
+    pdl_wait();
+    pdl_trigger();
     int ids[IPT];
 #pragma unroll
     for (int i = 0; i < IPT; ++i) {
@@ -1035,6 +1036,358 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs
         const int start = __shfl_sync(FULL_MASK, cu_e + tot_e, warp);
         const int end = __shfl_sync(FULL_MASK, cu_incl, warp);
         for (int j = start + lane; j < end; j += 32)
+            if (j >= 0 && static_cast<int64_t>(j) < a.p_cap) a.out.src_of_slot[j] = -1;
+    }
+    {
+        const uint32_t cap = static_cast<uint32_t>(a.p_cap);  // < 2^31
+        const uint32_t rest = cap - static_cast<uint32_t>(P);
+        const uint32_t share = (rest + ncta - 1u) / ncta;
+        const uint32_t b = static_cast<uint32_t>(P) + share * crank, e = min(cap, b + share);
+        for (uint32_t j = b + tid; j < e; j += PLAN_THREADS) a.out.src_of_slot[j] = -1;
+    }
+}
+
+// ---------------------------------------------------------------- medium-E path
+// 32 < E <= 32 * EW (EW = 4 or 8) and R <= 32: the small-E scheme with each
+// lane owning experts lane + 32 j (j < EW).  Per warp step, NBE ballots of
+// the experts' bits give lane x the lanes holding each of its experts (the
+// low five bits once, then one LOP per high bit and chunk); a pair's
+// running base within its warp run comes by shuffle from the owning lane.
+// After the first pass one CTA-wide column scan turns the [32 warps][E]
+// counts into warp bases: thread (e, q) scans expert e over warps
+// [8q, 8q + 8), a second barrier adds the quarter offsets and yields the
+// tile count, which the thread pushes into four CTAs of the cluster.  After
+// the cluster barrier threads e < E derive the expert's tile prefix and
+// total, warp 0 scans the padded totals into cu_seqlens, and the second
+// pass writes the slots.  Per-pair results stay in registers.
+template <int IPT, int EW>
+__global__ void __launch_bounds__(PLAN_THREADS) plan_medium_kernel(const PlanArgs a) {
+    constexpr int NBE = 5 + (EW == 8 ? 3 : 2);  // expert bits
+    constexpr int NBR = 5;                       // rank bits (R <= 32)
+    extern __shared__ __align__(16) int32_t s_dyn[];
+    const int E = a.E, K = a.K, R = a.R, C = a.C;
+    int32_t* s_wc = s_dyn;                       // [32][E]   per-warp pairs per expert, then warp bases
+    int32_t* s_qt = s_wc + PLAN_WARPS * E;       // [4][256]  per-quarter totals
+    int32_t* s_all = s_qt + 4 * 256;             // [16][C]   every tile's counts, pushed by its CTA
+    int32_t* s_base = s_all + 16 * C;            // [E]       cu[e] + pairs of e in lower tiles
+    int32_t* s_pad = s_base + E;                 // [E]       padded totals, then cu_seqlens
+    int32_t* s_tot = s_pad + E;                  // [E]       totals
+    __shared__ int32_t s_wr[PLAN_WARPS][SMALL_MAX + 1];
+    __shared__ int32_t s_wg[PLAN_WARPS], s_wd[PLAN_WARPS];
+    __shared__ int32_t s_gd[4];  // groups, duplicates of lower tiles; their totals
+    __shared__ int32_t s_P;
+
+    cluster_arrive_relaxed();  // this CTA has started: the others may push into it once all have
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t crank = cluster_ctarank(), ncta = cluster_nctarank();
+    const int tile = static_cast<int>(crank);
+    const int64_t tok0 = static_cast<int64_t>(tile) * a.tile_tokens;
+    const unsigned lt = (1u << lane) - 1u;
+    const int act = a.tpw * K;
+    const int tok_in_iter = lane / K, k = lane - tok_in_iter * K;
+    const int tok_lane0 = tok_in_iter * K;
+    const unsigned below_tok = (1u << tok_lane0) - 1u;
+    const unsigned seg = (K >= 32 ? FULL_MASK : ((1u << K) - 1u)) << tok_lane0;
+    const bool k_pow2 = (K & (K - 1)) == 0;
+    unsigned xl[5];
+#pragma unroll
+    for (int b = 0; b < 5; ++b) xl[b] = 0u - ((static_cast<unsigned>(lane) >> b) & 1u);
+
+    pdl_wait();
+    pdl_trigger();
+    int ids[IPT];
+#pragma unroll
+    for (int i = 0; i < IPT; ++i) {
+        const int64_t s = tok0 + static_cast<int64_t>(warp * IPT + i) * a.tpw + tok_in_iter;
+        ids[i] = (lane < act && s < a.N) ? __ldg(a.topk + s * K + k) : -1;
+    }
+
+    // ---- first pass, all in registers
+    int cnt[EW];
+#pragma unroll
+    for (int j = 0; j < EW; ++j) cnt[j] = 0;
+    int cnt_r = 0, run_g = 0, run_d = 0;
+    uint2 item[IPT];
+#pragma unroll
+    for (int i = 0; i < IPT; ++i) {
+        const int64_t s = tok0 + static_cast<int64_t>(warp * IPT + i) * a.tpw + tok_in_iter;
+        bool active = lane < act && s < a.N;
+        int e = 0;
+        if (active) {
+            e = ids[i];
+            if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
+                record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(s * K + k));
+                active = false;
+                e = 0;
+            }
+        }
+        const unsigned amask = __ballot_sync(FULL_MASK, active);
+        const int r = rank_of(a, e);
+        unsigned eb[NBE];
+        unsigned peers = amask, mlow = amask, pr = amask, mr = amask;
+#pragma unroll
+        for (int b = 0; b < NBE; ++b) {
+            eb[b] = __ballot_sync(FULL_MASK, (e >> b) & 1);
+            peers &= ~(eb[b] ^ (0u - ((e >> b) & 1)));
+            if (b < 5) mlow &= ~(eb[b] ^ xl[b]);  // lanes whose expert is lane (mod 32)
+        }
+#pragma unroll
+        for (int b = 0; b < NBR; ++b) {
+            const unsigned rb = __ballot_sync(FULL_MASK, (r >> b) & 1);
+            mr &= ~(rb ^ xl[b]);
+            pr &= ~(rb ^ (0u - ((r >> b) & 1)));
+        }
+        int base = 0;
+#pragma unroll
+        for (int j = 0; j < EW; ++j) {
+            unsigned m = mlow;  // lanes holding expert lane + 32 j
+#pragma unroll
+            for (int b = 5; b < NBE; ++b) m &= ((j >> (b - 5)) & 1) ? eb[b] : ~eb[b];
+            const int t = __shfl_sync(FULL_MASK, cnt[j], e & 31);
+            if ((e >> 5) == j) base = t;
+            cnt[j] += __popc(m);
+        }
+        const int wr = base + __popc(peers & lt);
+
+        const unsigned pd = pr & seg;  // this token's pairs on this lane's rank
+        const bool prim = active && (pd & lt) == 0u;
+        const bool dup = active && !prim;
+        const bool opens = prim && __popc(pd) >= 2;
+        const unsigned pmask = __ballot_sync(FULL_MASK, prim);
+        cnt_r += __popc(mr & pmask);
+        const unsigned gball = __ballot_sync(FULL_MASK, opens);
+        const unsigned dball = amask & ~pmask;
+        int groups_before = 0;
+        if (K > 2) {
+            const int my_p = __ffs(pd) - 1;
+            const int gsz = opens ? __popc(pd) - 1 : 0;
+            const int excl = warp_incl_scan(gsz, 32) - gsz;
+            const int tok_base = __shfl_sync(FULL_MASK, excl, tok_lane0 & 31);
+            groups_before = __shfl_sync(FULL_MASK, excl, my_p & 31) - tok_base;
+        }
+        const int before = groups_before + (dup ? __popc(pd & lt) - 1 : 0);
+        const int dup_pos = run_d + __popc(dball & below_tok) + before;
+
+        uint32_t rbits = prim ? 1u << r : 0u;
+        if (k_pow2) {
+            for (int off = 1; off < K; off <<= 1) rbits |= __shfl_xor_sync(FULL_MASK, rbits, off);
+        } else {
+            uint32_t acc = 0;
+            for (int q = 0; q < K; ++q) acc |= __shfl_sync(FULL_MASK, rbits, (tok_lane0 + q) & 31);
+            rbits = acc;
+        }
+        if (active && k == 0) store_rank_row(a.out.is_token_in_rank + s * R, rbits, R);
+
+        item[i] = active ? pack_item(e, wr, dup, opens, __popc(pd) - 1, opens ? run_g + __popc(gball & lt) : dup_pos,
+                                     dup_pos)
+                         : make_uint2(ITEM_NONE, 0u);
+        run_g += __popc(gball);
+        run_d += __popc(dball);
+    }
+#pragma unroll
+    for (int j = 0; j < EW; ++j)
+        if (lane + 32 * j < E) s_wc[warp * E + lane + 32 * j] = cnt[j];
+    s_wr[warp][lane] = cnt_r;
+    if (lane == 0) {
+        s_wg[warp] = run_g;
+        s_wd[warp] = run_d;
+    }
+    __syncthreads();
+    cluster_wait();  // every CTA of the cluster has started
+
+    // ---- column scan over warps: thread (e, q) takes warps [8q, 8q + 8)
+    const int ce = tid & 255, cq = tid >> 8;
+    int v[8];
+    int qsum = 0;
+    if (ce < E) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = s_wc[(8 * cq + i) * E + ce];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int c = v[i];
+            v[i] = qsum;  // exclusive within the quarter
+            qsum += c;
+        }
+        s_qt[cq * 256 + ce] = qsum;
+    }
+    // groups and duplicates: warp 1 scans the warp runs (bases kept in s_wg / s_wd)
+    if (warp == 1) {
+        const int g = s_wg[lane], d = s_wd[lane];
+        const int gi = warp_incl_scan(g, 32), di = warp_incl_scan(d, 32);
+        s_wg[lane] = gi - g;
+        s_wd[lane] = di - d;
+        if (lane == 31) {
+            s_gd[2] = gi;  // this tile's groups and duplicates
+            s_gd[3] = di;
+        }
+    }
+    int tile_r = 0;
+    if (warp == 2) {
+#pragma unroll 8
+        for (int w = 0; w < PLAN_WARPS; ++w) tile_r += s_wr[w][lane];
+    }
+    __syncthreads();
+
+    // ---- quarter offsets -> warp bases; tile counts pushed to the cluster
+    if (ce < E) {
+        int qoff = 0, tile_e = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int t = s_qt[q * 256 + ce];
+            qoff += q < cq ? t : 0;
+            tile_e += t;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s_wc[(8 * cq + i) * E + ce] = v[i] + qoff;
+        for (uint32_t q = static_cast<uint32_t>(cq); q < ncta; q += 4)
+            st_dsmem_s32(dsmem_addr(s_all + tile * C + ce, q), tile_e);
+    }
+    if (warp == 2) {  // ranks: lane r pushes to every CTA
+        if (lane < R)
+            for (uint32_t q = 0; q < ncta; ++q) st_dsmem_s32(dsmem_addr(s_all + tile * C + E + lane, q), tile_r);
+    }
+    if (warp == 3 && static_cast<uint32_t>(lane) < ncta) {  // groups, duplicates: lane q pushes to CTA q
+        st_dsmem_s32(dsmem_addr(s_all + tile * C + E + R, lane), s_gd[2]);
+        st_dsmem_s32(dsmem_addr(s_all + tile * C + E + R + 1, lane), s_gd[3]);
+    }
+    cluster_arrive();  // release: this CTA's pushes
+    cluster_wait();    // acquire: every tile's counts are in s_all
+
+    // ---- lower tiles and totals per expert; groups / duplicates of lower tiles
+    const int al = a.alignment;
+    for (int e = tid; e < E; e += PLAN_THREADS) {
+        int pre = 0, tot = 0;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const int t = q < static_cast<int>(ncta) ? s_all[q * C + e] : 0;
+            pre += q < tile ? t : 0;
+            tot += t;
+        }
+        s_base[e] = pre;
+        s_tot[e] = tot;
+        const unsigned u = static_cast<unsigned>(tot) + static_cast<unsigned>(al) - 1u;
+        const unsigned alu = static_cast<unsigned>(al);
+        s_pad[e] = tot > 0 ? static_cast<int>((alu & (alu - 1u)) == 0u ? (u & ~(alu - 1u)) : u / alu * alu) : 0;
+    }
+    if (warp == PLAN_WARPS - 1) {
+        const int gq = static_cast<uint32_t>(lane) < ncta ? s_all[lane * C + E + R] : 0;
+        const int dq = static_cast<uint32_t>(lane) < ncta ? s_all[lane * C + E + R + 1] : 0;
+        const int gp = __reduce_add_sync(FULL_MASK, lane < tile ? gq : 0);
+        const int dp = __reduce_add_sync(FULL_MASK, lane < tile ? dq : 0);
+        const int gt = __reduce_add_sync(FULL_MASK, gq), dt = __reduce_add_sync(FULL_MASK, dq);
+        if (lane == 0) {
+            s_gd[0] = gp;
+            s_gd[1] = dp;
+            if (tile == 0) {
+                a.out.dup_counts[0] = gt;
+                a.out.dup_counts[1] = dt;
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- warp 0: cu_seqlens (lane l scans experts [l * EW, l * EW + EW)),
+    // tile 0 also the totals-derived outputs
+    if (warp == 0) {
+        int pv[EW], run = 0;
+#pragma unroll
+        for (int j = 0; j < EW; ++j) {
+            const int e = lane * EW + j;
+            pv[j] = e < E ? s_pad[e] : 0;
+            run += pv[j];
+        }
+        const int incl = warp_incl_scan(run, 32);
+        int c = incl - run;
+        const int P = __shfl_sync(FULL_MASK, incl, 31);
+#pragma unroll
+        for (int j = 0; j < EW; ++j) {
+            const int e = lane * EW + j;
+            if (e < E) {
+                if (tile == 0) {
+                    const int tot = s_tot[e];
+                    a.out.tokens_per_expert[e] = tot;
+                    a.out.cu_seqlens[e] = c;
+                    const int pad = pv[j] - tot;
+                    a.out.zero_fill_ranges[2 * e] = pad > 0 ? c + tot : 0;
+                    a.out.zero_fill_ranges[2 * e + 1] = pad > 0 ? pad : 0;
+                }
+                s_base[e] += c;
+                s_pad[e] = c;  // s_pad now holds cu_seqlens
+            }
+            c += pv[j];
+        }
+        if (lane == 0) s_P = P;
+        if (tile == 0 && lane == 0) {
+            a.out.cu_seqlens[E] = P;
+            a.out.rank_slot_offsets[R] = P;
+        }
+    }
+    __syncthreads();
+    const int P = s_P;
+
+    if (tile == 0 && warp == 1) {  // rank arrays (DeepEP notify_dispatch rank prefix)
+        int tot_r = 0;
+        if (lane < R)
+            for (int q = 0; q < static_cast<int>(ncta); ++q) tot_r += s_all[q * C + E + lane];
+        const int incl = warp_incl_scan(tot_r, 32);
+        const int total = __shfl_sync(FULL_MASK, incl, 31);
+        if (lane < R) {
+            int ppr = 0;
+            for (int e = lane * a.epn; e < (lane + 1) * a.epn; ++e) ppr += s_tot[e];
+            a.out.rank_slot_offsets[lane] = s_pad[lane * a.epn];
+            a.out.pairs_per_rank[lane] = ppr;
+            a.out.tokens_per_rank[lane] = tot_r;
+            a.out.rank_prefix[lane] = incl - tot_r;
+        }
+        if (lane == 0) a.out.rank_prefix[R] = total;
+    }
+
+    // ---- second pass: slots, dst, src_of_slot, dedup structures
+    const int64_t gbase = static_cast<int64_t>(s_gd[0]) + s_wg[warp];
+    const int64_t dbase = static_cast<int64_t>(s_gd[1]) + s_wd[warp];
+#pragma unroll
+    for (int i = 0; i < IPT; ++i) {
+        const uint2 it = item[i];
+        const uint32_t e = it.x & 0x7ffu;
+        if (e == ITEM_NONE) continue;
+        const int64_t s = tok0 + static_cast<int64_t>(warp * IPT + i) * a.tpw + tok_in_iter;
+        const int64_t f = s * K + k;
+        const int32_t slot = s_base[e] + s_wc[warp * E + e] + static_cast<int32_t>((it.x >> 11) & 0x3ffu);
+        if (slot < 0 || static_cast<int64_t>(slot) >= a.p_cap) {
+            record_error(a.out.status, MOE_ERR_DEVICE_INDEX, slot);
+            continue;
+        }
+        const bool dup = (it.x >> 21) & 1u;
+        const bool opens = (it.x >> 22) & 1u;
+        const int32_t ia = static_cast<int32_t>(it.y & 0xffffu), ib = static_cast<int32_t>(it.y >> 16);
+        a.out.dst[f] = dup ? -slot - 1 : slot;
+        a.out.src_of_slot[slot] = static_cast<int32_t>(f);
+        if (opens) {
+            const int64_t g = gbase + ia;
+            if (g >= static_cast<int64_t>(a.N) * (K / 2)) {
+                record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(g));
+                continue;
+            }
+            int32_t* row = a.out.dup_groups + 3 * g;
+            row[0] = slot;
+            row[1] = static_cast<int32_t>(dbase + ib);
+            row[2] = static_cast<int32_t>(it.x >> 23);
+        } else if (dup) {
+            const int64_t pos = dbase + ia;
+            if (pos >= static_cast<int64_t>(a.N) * (K - 1)) {
+                record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(pos));
+                continue;
+            }
+            a.out.dup_loffs[pos] = slot;
+        }
+    }
+
+    // ---- -1 into the padding rows (experts tile, tile + T, ...: a warp
+    // each) and into this tile's share of the unused rows [P, P_cap)
+    for (int e = tile + static_cast<int>(ncta) * warp; e < E; e += static_cast<int>(ncta) * PLAN_WARPS) {
+        const int cu = s_pad[e], tot = s_tot[e];
+        const int end = e + 1 < E ? s_pad[e + 1] : P;
+        for (int j = cu + tot + lane; j < end; j += 32)
             if (j >= 0 && static_cast<int64_t>(j) < a.p_cap) a.out.src_of_slot[j] = -1;
     }
     {
@@ -1350,6 +1703,45 @@ bool small_geometry(int N, int E, int K, int R, Geom* g) {
     return false;
 }
 
+// ---- medium-E path geometry: 32 < E <= 256, R <= 32, 32 warps per CTA,
+// the fewest warp steps (1, 2, 4) that keep the tiles within 16.
+bool medium_geometry(int N, int E, int K, int R, Geom* g) {
+    if (E <= moe::SMALL_MAX || E > 256 || R > moe::SMALL_MAX) return false;
+    g->tpw = 32 / K;
+    g->C = E + R + 2;
+    for (int ipt : {1, 2, 4}) {
+        g->ipt = ipt;
+        g->tile_tokens = moe::PLAN_WARPS * ipt * g->tpw;
+        const int64_t T = (static_cast<int64_t>(N) + g->tile_tokens - 1) / g->tile_tokens;
+        if (T <= kMaxClusterTiles) {
+            g->T = static_cast<int>(T);
+            return true;
+        }
+    }
+    return false;
+}
+
+size_t medium_smem(const Geom& g, int E) {
+    return sizeof(int32_t) * (static_cast<size_t>(moe::PLAN_WARPS) * E + 4 * 256 + 16 * static_cast<size_t>(g.C) + 3 * E);
+}
+
+// EW = 4 when E <= 128, else 8.
+template <typename F>
+auto with_medium_kernel(int ipt, int E, F&& f) {
+    if (E <= 128) {
+        switch (ipt) {
+            case 1: return f(moe::plan_medium_kernel<1, 4>);
+            case 2: return f(moe::plan_medium_kernel<2, 4>);
+            default: return f(moe::plan_medium_kernel<4, 4>);
+        }
+    }
+    switch (ipt) {
+        case 1: return f(moe::plan_medium_kernel<1, 8>);
+        case 2: return f(moe::plan_medium_kernel<2, 8>);
+        default: return f(moe::plan_medium_kernel<4, 8>);
+    }
+}
+
 // NB = 3 when E <= 8 (so R <= 8), else 5.
 template <typename F>
 auto with_small_kernel(int ipt, int E, F&& f) {
@@ -1483,7 +1875,19 @@ int ensure_kernel_attributes() {
             cudaFuncSetAttribute(moe::plan_small_kernel<1, 5>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
             cudaFuncSetAttribute(moe::plan_small_kernel<2, 5>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
             cudaFuncSetAttribute(moe::plan_small_kernel<4, 5>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
-            cudaFuncSetAttribute(moe::plan_small_kernel<8, 5>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)};
+            cudaFuncSetAttribute(moe::plan_small_kernel<8, 5>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_medium_kernel<1, 4>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_medium_kernel<2, 4>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_medium_kernel<4, 4>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_medium_kernel<1, 8>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_medium_kernel<2, 8>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_medium_kernel<4, 8>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_medium_kernel<1, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, big),
+            cudaFuncSetAttribute(moe::plan_medium_kernel<2, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, big),
+            cudaFuncSetAttribute(moe::plan_medium_kernel<4, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, big),
+            cudaFuncSetAttribute(moe::plan_medium_kernel<1, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, big),
+            cudaFuncSetAttribute(moe::plan_medium_kernel<2, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, big),
+            cudaFuncSetAttribute(moe::plan_medium_kernel<4, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, big)};
         cudaError_t first = cudaSuccess;
         for (cudaError_t e : errs)
             if (first == cudaSuccess) first = e;
@@ -1493,10 +1897,10 @@ int ensure_kernel_attributes() {
 }
 
 // Which path a plan of these sizes takes on the current device.  Default
-// order: the small-E cluster kernel, then the two-launch look-back plan.
-// MOE_PLAN_PATH=small|cluster|grid|lookback forces a path where the sizes
-// allow it (the look-back plan otherwise).
-enum PlanPath { PATH_SMALL = 0, PATH_CLUSTER = 1, PATH_GRID = 2, PATH_LOOKBACK = 3 };
+// order: the small-E cluster kernel, the medium-E cluster kernel, then the
+// two-launch look-back plan.  MOE_PLAN_PATH=small|medium|cluster|grid|lookback
+// forces a path where the sizes allow it (the look-back plan otherwise).
+enum PlanPath { PATH_SMALL = 0, PATH_CLUSTER = 1, PATH_GRID = 2, PATH_LOOKBACK = 3, PATH_MEDIUM = 4 };
 
 struct PathChoice {
     int path;
@@ -1514,6 +1918,11 @@ PathChoice choose_path(int N, int E, int K, int R) {
     if ((any || want == "small") && small_geometry(N, E, K, R, &g)) {
         const bool ok = with_small_kernel(g.ipt, E, [&](auto kern) { return cluster_launchable(kern, g.T, 0); });
         if (ok) return PathChoice{PATH_SMALL, g, moe::PLAN_WARPS, 0};
+    }
+    if ((any || want == "medium") && medium_geometry(N, E, K, R, &g)) {
+        const size_t smem = medium_smem(g, E);
+        const bool ok = with_medium_kernel(g.ipt, E, [&](auto kern) { return cluster_launchable(kern, g.T, smem); });
+        if (ok) return PathChoice{PATH_MEDIUM, g, moe::PLAN_WARPS, smem};
     }
     if (want == "cluster" && cluster_geometry(N, E, K, R, &g)) {
         const size_t smem = cluster_smem(g, E, R);
@@ -1597,6 +2006,9 @@ extern "C" MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, in
     // ---- one launch: a thread-block cluster of up to 16 tiles, E, R <= 32
     if (pc.path == PATH_SMALL)
         return with_small_kernel(g.ipt, E, [&](auto kern) { return launch_cluster(kern, a, 0, stream); });
+    // ---- one launch: a thread-block cluster of up to 16 tiles, 32 < E <= 256, R <= 32
+    if (pc.path == PATH_MEDIUM)
+        return with_medium_kernel(g.ipt, E, [&](auto kern) { return launch_cluster(kern, a, pc.smem, stream); });
     // ---- one launch: a thread-block cluster of up to 16 tiles, any E
     if (pc.path == PATH_CLUSTER) return launch_cluster(moe::plan_cluster_kernel, a, pc.smem, stream);
     // ---- one launch over the whole GPU, all tiles resident at once

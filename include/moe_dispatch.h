@@ -145,13 +145,14 @@ MOE_API size_t moe_plan_workspace_size(int N, int E, int K, int R);
 
 /*
  * Kernel launches moe_plan makes for these sizes on the current device: 1
- * when E <= 32, R <= 32 and the plan fits one thread-block cluster of up to
- * 16 tiles (one tile = 32 warps x 1, 2, 4 or 8 steps x floor(32/K) tokens)
- * that the GPU can co-schedule, else 2 (decoupled look-back, then the
- * scatter).  -1 on bad sizes.  The environment variable
- * MOE_PLAN_PATH=small|cluster|grid|lookback forces a path where the sizes
- * allow it (cluster: a one-launch cluster plan for any E; grid: one launch
- * of up to 152 co-resident tiles); every path produces the identical plan.
+ * when R <= 32, E <= 256 and the plan fits one thread-block cluster of up to
+ * 16 tiles (one tile = 32 warps x 1, 2, 4 or 8 steps x floor(32/K) tokens;
+ * at most 4 steps when E > 32) that the GPU can co-schedule, else 2
+ * (decoupled look-back, then the scatter).  -1 on bad sizes.  The
+ * environment variable MOE_PLAN_PATH=small|medium|cluster|grid|lookback
+ * forces a path where the sizes allow it (cluster: a one-launch cluster
+ * plan for any E; grid: one launch of up to 152 co-resident tiles); every
+ * path produces the identical plan.
  */
 MOE_API int moe_plan_launch_count(int N, int E, int K, int R);
 

@@ -118,12 +118,13 @@ def plan_both(m, topk, E, R, a, out=None):
     return p, got, want
 
 
-@pytest.fixture(params=["small", "cluster", "grid", "lookback"])
+@pytest.fixture(params=["small", "medium", "cluster", "grid", "lookback"])
 def plan_path(request, monkeypatch):
     """Force one plan path where the sizes allow it (the two-launch look-back
-    plan otherwise): small = the E, R <= 32 cluster kernel (the default where
-    it applies), cluster = the general cluster kernel, grid = one launch over
-    all SMs with every tile resident, lookback = the two-launch plan."""
+    plan otherwise): small = the E, R <= 32 cluster kernel and medium = the
+    32 < E <= 256, R <= 32 one (the defaults where they apply), cluster = the
+    general cluster kernel, grid = one launch over all SMs with every tile
+    resident, lookback = the two-launch plan."""
     monkeypatch.setenv("MOE_PLAN_PATH", request.param)
     return request.param
 
@@ -179,6 +180,7 @@ def test_plan_workspace_reuse_across_calls_and_sizes(m, plan_path):
 
 def test_plan_launch_counts(m, monkeypatch):
     assert m.plan_launches(16384, 8, 2, 4) == 1          # small-E cluster kernel
+    assert m.plan_launches(8192, 128, 8, 8) == 1         # medium-E cluster kernel
     assert m.plan_launches(65536, 256, 8, 64) == 2       # look-back plan
     monkeypatch.setenv("MOE_PLAN_PATH", "lookback")
     assert m.plan_launches(16384, 8, 2, 4) == 2
