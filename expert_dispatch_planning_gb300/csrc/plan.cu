@@ -736,10 +736,10 @@ __device__ __forceinline__ int warp_incl_scan(int v, int width) {
 // is_token_in_rank row of one token from its rank bitmask (bytes 0 / 1).
 __device__ __forceinline__ void store_rank_row(uint8_t* row, uint32_t mask, int R) {
     if ((R & 3) == 0 && (reinterpret_cast<uintptr_t>(row) & 3u) == 0) {
-        for (int c = 0; c < R / 4; ++c) {
-            const uint32_t m = mask >> (4 * c);
-            reinterpret_cast<uint32_t*>(row)[c] = (m & 1u) | ((m & 2u) << 7) | ((m & 4u) << 14) | ((m & 8u) << 21);
-        }
+        // bit i of a 4-bit m to byte i: m * (1 + 2^7 + 2^14 + 2^21) places
+        // copies of m 7 bits apart (no carries), the mask keeps bit i of copy i
+        for (int c = 0; c < R / 4; ++c)
+            reinterpret_cast<uint32_t*>(row)[c] = (((mask >> (4 * c)) & 15u) * 0x204081u) & 0x01010101u;
     } else {
         for (int x = 0; x < R; ++x) row[x] = static_cast<uint8_t>((mask >> x) & 1u);
     }
@@ -762,7 +762,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs
     const int E = a.E, K = a.K, R = a.R;
     const uint32_t crank = cluster_ctarank(), ncta = cluster_nctarank();
     const int tile = static_cast<int>(crank);
-    const int64_t tok0 = static_cast<int64_t>(tile) * a.tile_tokens;
+    const int tok0 = tile * a.tile_tokens;  // N * K < 2^30: token and pair indices fit in int
     const unsigned lt = (1u << lane) - 1u;
     const int act = a.tpw * K;
     const int tok_in_iter = lane / K, k = lane - tok_in_iter * K;
@@ -779,7 +779,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs
     int ids[IPT];
 #pragma unroll
     for (int i = 0; i < IPT; ++i) {
-        const int64_t s = tok0 + static_cast<int64_t>(warp * IPT + i) * a.tpw + tok_in_iter;
+        const int s = tok0 + (warp * IPT + i) * a.tpw + tok_in_iter;
         ids[i] = (lane < act && s < a.N) ? __ldg(a.topk + s * K + k) : -1;
     }
 
@@ -788,13 +788,13 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs
     uint2 item[IPT];
 #pragma unroll
     for (int i = 0; i < IPT; ++i) {
-        const int64_t s = tok0 + static_cast<int64_t>(warp * IPT + i) * a.tpw + tok_in_iter;
+        const int s = tok0 + (warp * IPT + i) * a.tpw + tok_in_iter;
         bool active = lane < act && s < a.N;
         int e = 0;
         if (active) {
             e = ids[i];
             if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
-                record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(s * K + k));
+                record_error(a.out.status, MOE_ERR_DEVICE_INDEX, s * K + k);
                 active = false;
                 e = 0;
             }
@@ -847,7 +847,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs
             for (int q = 0; q < K; ++q) acc |= __shfl_sync(FULL_MASK, rbits, (tok_lane0 + q) & 31);
             rbits = acc;
         }
-        if (active && k == 0) store_rank_row(a.out.is_token_in_rank + s * R, rbits, R);
+        if (active && k == 0) store_rank_row(a.out.is_token_in_rank + static_cast<int64_t>(s) * R, rbits, R);
 
         item[i] = active ? pack_item(e, wr, dup, opens, __popc(pd) - 1, opens ? run_g + __popc(gball & lt) : dup_pos,
                                      dup_pos)
@@ -957,8 +957,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs
         const uint32_t e = it.x & 0x7ffu;
         const int sb = __shfl_sync(FULL_MASK, slot_base, static_cast<int>(e & 31u));
         if (e == ITEM_NONE) continue;
-        const int64_t s = tok0 + static_cast<int64_t>(warp * IPT + i) * a.tpw + tok_in_iter;
-        const int64_t f = s * K + k;
+        const int s = tok0 + (warp * IPT + i) * a.tpw + tok_in_iter;
+        const int f = s * K + k;
         const int32_t slot = sb + static_cast<int32_t>((it.x >> 11) & 0x3ffu);
         if (slot < 0 || static_cast<int64_t>(slot) >= a.p_cap) {
             record_error(a.out.status, MOE_ERR_DEVICE_INDEX, slot);
@@ -968,7 +968,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs
         const bool opens = (it.x >> 22) & 1u;
         const int32_t ia = static_cast<int32_t>(it.y & 0xffffu), ib = static_cast<int32_t>(it.y >> 16);
         a.out.dst[f] = dup ? -slot - 1 : slot;
-        a.out.src_of_slot[slot] = static_cast<int32_t>(f);
+        a.out.src_of_slot[slot] = f;
         if (opens) {
             const int64_t g = gbase + ia;
             if (g >= static_cast<int64_t>(a.N) * (K / 2)) {
@@ -1048,11 +1048,12 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs
 }
 
 // ---------------------------------------------------------------- medium-E path
-// 32 < E <= 32 * EW (EW = 4 or 8) and R <= 32: the small-E scheme with each
-// lane owning experts lane + 32 j (j < EW).  Per warp step, NBE ballots of
-// the experts' bits give lane x the lanes holding each of its experts (the
-// low five bits once, then one LOP per high bit and chunk); a pair's
-// running base within its warp run comes by shuffle from the owning lane.
+// 32 < E <= 32 * EW (EW = 4 or 8) and R <= 32: the small-E scheme, except
+// that each warp keeps its running pairs per expert in a shared-memory row:
+// per warp step, match.any gives a pair the lanes holding its expert (at
+// this E cheaper than the bit ballots: the step is bound by the integer
+// pipe), it reads its expert's running count (lanes of a group read one
+// word) and the group's first lane writes the new count back.
 // After the first pass one CTA-wide column scan turns the [32 warps][E]
 // counts into warp bases: thread (e, q) scans expert e over warps
 // [8q, 8q + 8), a second barrier adds the quarter offsets and yields the
@@ -1062,8 +1063,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs
 // pass writes the slots.  Per-pair results stay in registers.
 template <int IPT, int EW>
 __global__ void __launch_bounds__(PLAN_THREADS) plan_medium_kernel(const PlanArgs a) {
-    constexpr int NBE = 5 + (EW == 8 ? 3 : 2);  // expert bits
-    constexpr int NBR = 5;                       // rank bits (R <= 32)
+    constexpr int NBR = 5;  // rank bits (R <= 32)
     extern __shared__ __align__(16) int32_t s_dyn[];
     const int E = a.E, K = a.K, R = a.R, C = a.C;
     int32_t* s_wc = s_dyn;                       // [32][E]   per-warp pairs per expert, then warp bases
@@ -1072,6 +1072,9 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_medium_kernel(const PlanArg
     int32_t* s_base = s_all + 16 * C;            // [E]       cu[e] + pairs of e in lower tiles
     int32_t* s_pad = s_base + E;                 // [E]       padded totals, then cu_seqlens
     int32_t* s_tot = s_pad + E;                  // [E]       totals
+    int32_t* s_src = s_tot + E;                  // [32 * IPT * 32] the tile's pairs in slot order: f
+    int32_t* s_gsl = s_src + PLAN_WARPS * 32 * IPT;  // [32 * IPT * 32] ... and their slots
+    int32_t* s_tloc = s_qt;                      // [E + 1]   tile-local first pair per expert (after the exchange)
     __shared__ int32_t s_wr[PLAN_WARPS][SMALL_MAX + 1];
     __shared__ int32_t s_wg[PLAN_WARPS], s_wd[PLAN_WARPS];
     __shared__ int32_t s_gd[4];  // groups, duplicates of lower tiles; their totals
@@ -1081,7 +1084,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_medium_kernel(const PlanArg
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t crank = cluster_ctarank(), ncta = cluster_nctarank();
     const int tile = static_cast<int>(crank);
-    const int64_t tok0 = static_cast<int64_t>(tile) * a.tile_tokens;
+    const int tok0 = tile * a.tile_tokens;  // N * K < 2^30: token and pair indices fit in int
     const unsigned lt = (1u << lane) - 1u;
     const int act = a.tpw * K;
     const int tok_in_iter = lane / K, k = lane - tok_in_iter * K;
@@ -1092,61 +1095,52 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_medium_kernel(const PlanArg
     unsigned xl[5];
 #pragma unroll
     for (int b = 0; b < 5; ++b) xl[b] = 0u - ((static_cast<unsigned>(lane) >> b) & 1u);
+    const int rbits = R > 1 ? 32 - __clz(R - 1) : 0;  // rank bits in use
+    int32_t* wrow = s_wc + warp * E;  // this warp's running pairs per expert
+    for (int e = lane; e < E; e += 32) wrow[e] = 0;
+    __syncwarp();
 
     pdl_wait();
     pdl_trigger();
     int ids[IPT];
 #pragma unroll
     for (int i = 0; i < IPT; ++i) {
-        const int64_t s = tok0 + static_cast<int64_t>(warp * IPT + i) * a.tpw + tok_in_iter;
+        const int s = tok0 + (warp * IPT + i) * a.tpw + tok_in_iter;
         ids[i] = (lane < act && s < a.N) ? __ldg(a.topk + s * K + k) : -1;
     }
 
-    // ---- first pass, all in registers
-    int cnt[EW];
-#pragma unroll
-    for (int j = 0; j < EW; ++j) cnt[j] = 0;
+    // ---- first pass: per-pair results in registers, running counts per
+    // expert in the warp's shared row (the group's first lane writes back)
     int cnt_r = 0, run_g = 0, run_d = 0;
     uint2 item[IPT];
 #pragma unroll
     for (int i = 0; i < IPT; ++i) {
-        const int64_t s = tok0 + static_cast<int64_t>(warp * IPT + i) * a.tpw + tok_in_iter;
+        const int s = tok0 + (warp * IPT + i) * a.tpw + tok_in_iter;
         bool active = lane < act && s < a.N;
         int e = 0;
         if (active) {
             e = ids[i];
             if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
-                record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(s * K + k));
+                record_error(a.out.status, MOE_ERR_DEVICE_INDEX, s * K + k);
                 active = false;
                 e = 0;
             }
         }
         const unsigned amask = __ballot_sync(FULL_MASK, active);
         const int r = rank_of(a, e);
-        unsigned eb[NBE];
-        unsigned peers = amask, mlow = amask, pr = amask, mr = amask;
-#pragma unroll
-        for (int b = 0; b < NBE; ++b) {
-            eb[b] = __ballot_sync(FULL_MASK, (e >> b) & 1);
-            peers &= ~(eb[b] ^ (0u - ((e >> b) & 1)));
-            if (b < 5) mlow &= ~(eb[b] ^ xl[b]);  // lanes whose expert is lane (mod 32)
-        }
+        // with E in the hundreds one match beats NBE ballots and their LOPs
+        const unsigned peers = __match_any_sync(FULL_MASK, active ? e : -1);
+        unsigned pr = amask, mr = amask;
 #pragma unroll
         for (int b = 0; b < NBR; ++b) {
-            const unsigned rb = __ballot_sync(FULL_MASK, (r >> b) & 1);
+            const unsigned rb = b < rbits ? __ballot_sync(FULL_MASK, (r >> b) & 1) : 0u;
             mr &= ~(rb ^ xl[b]);
             pr &= ~(rb ^ (0u - ((r >> b) & 1)));
         }
-        int base = 0;
-#pragma unroll
-        for (int j = 0; j < EW; ++j) {
-            unsigned m = mlow;  // lanes holding expert lane + 32 j
-#pragma unroll
-            for (int b = 5; b < NBE; ++b) m &= ((j >> (b - 5)) & 1) ? eb[b] : ~eb[b];
-            const int t = __shfl_sync(FULL_MASK, cnt[j], e & 31);
-            if ((e >> 5) == j) base = t;
-            cnt[j] += __popc(m);
-        }
+        const int base = active ? wrow[e] : 0;
+        __syncwarp();
+        if (active && (peers & lt) == 0u) wrow[e] = base + __popc(peers);
+        __syncwarp();
         const int wr = base + __popc(peers & lt);
 
         const unsigned pd = pr & seg;  // this token's pairs on this lane's rank
@@ -1176,7 +1170,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_medium_kernel(const PlanArg
             for (int q = 0; q < K; ++q) acc |= __shfl_sync(FULL_MASK, rbits, (tok_lane0 + q) & 31);
             rbits = acc;
         }
-        if (active && k == 0) store_rank_row(a.out.is_token_in_rank + s * R, rbits, R);
+        if (active && k == 0) store_rank_row(a.out.is_token_in_rank + static_cast<int64_t>(s) * R, rbits, R);
 
         item[i] = active ? pack_item(e, wr, dup, opens, __popc(pd) - 1, opens ? run_g + __popc(gball & lt) : dup_pos,
                                      dup_pos)
@@ -1184,9 +1178,6 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_medium_kernel(const PlanArg
         run_g += __popc(gball);
         run_d += __popc(dball);
     }
-#pragma unroll
-    for (int j = 0; j < EW; ++j)
-        if (lane + 32 * j < E) s_wc[warp * E + lane + 32 * j] = cnt[j];
     s_wr[warp][lane] = cnt_r;
     if (lane == 0) {
         s_wg[warp] = run_g;
@@ -1289,16 +1280,27 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_medium_kernel(const PlanArg
     // ---- warp 0: cu_seqlens (lane l scans experts [l * EW, l * EW + EW)),
     // tile 0 also the totals-derived outputs
     if (warp == 0) {
-        int pv[EW], run = 0;
+        int pv[EW], tv[EW], run = 0, trun = 0;
 #pragma unroll
         for (int j = 0; j < EW; ++j) {
             const int e = lane * EW + j;
             pv[j] = e < E ? s_pad[e] : 0;
+            tv[j] = e < E ? s_all[tile * C + e] : 0;
             run += pv[j];
+            trun += tv[j];
         }
         const int incl = warp_incl_scan(run, 32);
         int c = incl - run;
         const int P = __shfl_sync(FULL_MASK, incl, 31);
+        const int tincl = warp_incl_scan(trun, 32);
+        int tl = tincl - trun;
+#pragma unroll
+        for (int j = 0; j < EW; ++j) {
+            const int e = lane * EW + j;
+            if (e < E) s_tloc[e] = tl;
+            tl += tv[j];
+        }
+        if (lane == 31) s_tloc[E] = tincl;
 #pragma unroll
         for (int j = 0; j < EW; ++j) {
             const int e = lane * EW + j;
@@ -1350,18 +1352,20 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_medium_kernel(const PlanArg
         const uint2 it = item[i];
         const uint32_t e = it.x & 0x7ffu;
         if (e == ITEM_NONE) continue;
-        const int64_t s = tok0 + static_cast<int64_t>(warp * IPT + i) * a.tpw + tok_in_iter;
-        const int64_t f = s * K + k;
-        const int32_t slot = s_base[e] + s_wc[warp * E + e] + static_cast<int32_t>((it.x >> 11) & 0x3ffu);
+        const int s = tok0 + (warp * IPT + i) * a.tpw + tok_in_iter;
+        const int f = s * K + k;
+        const int32_t in_tile = s_wc[warp * E + e] + static_cast<int32_t>((it.x >> 11) & 0x3ffu);
+        const int32_t slot = s_base[e] + in_tile;
         if (slot < 0 || static_cast<int64_t>(slot) >= a.p_cap) {
             record_error(a.out.status, MOE_ERR_DEVICE_INDEX, slot);
             continue;
         }
+        s_src[s_tloc[e] + in_tile] = f;
+        s_gsl[s_tloc[e] + in_tile] = slot;
         const bool dup = (it.x >> 21) & 1u;
         const bool opens = (it.x >> 22) & 1u;
         const int32_t ia = static_cast<int32_t>(it.y & 0xffffu), ib = static_cast<int32_t>(it.y >> 16);
         a.out.dst[f] = dup ? -slot - 1 : slot;
-        a.out.src_of_slot[slot] = static_cast<int32_t>(f);
         if (opens) {
             const int64_t g = gbase + ia;
             if (g >= static_cast<int64_t>(a.N) * (K / 2)) {
@@ -1381,6 +1385,12 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_medium_kernel(const PlanArg
             a.out.dup_loffs[pos] = slot;
         }
     }
+
+    // ---- src_of_slot: each expert's pairs of this tile are one run of
+    // slots, staged in slot order, so neighbouring threads store
+    // neighbouring slots
+    __syncthreads();
+    for (int i = tid; i < s_tloc[E]; i += PLAN_THREADS) a.out.src_of_slot[s_gsl[i]] = s_src[i];
 
     // ---- -1 into the padding rows (experts tile, tile + T, ...: a warp
     // each) and into this tile's share of the unused rows [P, P_cap)
@@ -1722,7 +1732,8 @@ bool medium_geometry(int N, int E, int K, int R, Geom* g) {
 }
 
 size_t medium_smem(const Geom& g, int E) {
-    return sizeof(int32_t) * (static_cast<size_t>(moe::PLAN_WARPS) * E + 4 * 256 + 16 * static_cast<size_t>(g.C) + 3 * E);
+    return sizeof(int32_t) * (static_cast<size_t>(moe::PLAN_WARPS) * E + 4 * 256 + 16 * static_cast<size_t>(g.C) +
+                              3 * static_cast<size_t>(E) + 2 * static_cast<size_t>(moe::PLAN_WARPS) * 32 * g.ipt);
 }
 
 // EW = 4 when E <= 128, else 8.
