@@ -8,8 +8,8 @@
 // by the bulk-copy engine: one cp.async.bulk global->shared load per group of
 // tokens (completion on an mbarrier, together with the 4-byte cp.async loads
 // of the group's dst entries), then one cp.async.bulk shared->global store
-// per pair.  A persistent single-warp CTA keeps a ring of stages in flight;
-// several CTAs share an SM.
+// per pair.  A single-warp CTA keeps a ring of stages in flight; many small
+// CTAs share an SM.
 //
 // moe_combine: out[s] = bf16(sum_k w[s,k] * y[slot(s,k)]) accumulated in
 // fp32, one fused multiply-add per pair in k order, rounded to nearest even
@@ -94,7 +94,6 @@ __global__ void __launch_bounds__(32) permute_kernel(const PermuteArgs a) {
         for (; issued < a.stages && issued < n_mine; ++issued) issue_x(issued);
 
     pdl_wait();
-    pdl_trigger();
     if (ld_volatile_s32(a.status) != 0) {  // no valid plan to move rows by
         // complete the prefetched stages and let their rows land before the
         // CTA releases its shared memory
@@ -139,6 +138,10 @@ __global__ void __launch_bounds__(32) permute_kernel(const PermuteArgs a) {
             }
         }
     }
+    // The next kernel (normally the combine, whose CTAs fill whole SMs) is
+    // let in only once this CTA's rows are on their way: dependents resident
+    // early slowed the last CTAs' stages (measured: up to 8% of a large step).
+    pdl_trigger();
     bulk_wait_read<0>();
     __syncwarp();
     if (failed) {
@@ -333,11 +336,14 @@ extern "C" MOE_API int moe_permute(const uint16_t* x, int N, int H, int K, int E
     a.E = E;
     a.alignment = alignment;
     a.p_cap = p_cap;
-    // Stages of ~32 KB, as many as fit one CTA's shared memory, and a grid of
-    // several CTAs per SM (only one is resident at a time): a deep ring keeps
-    // enough bytes in flight per SM, and the extra CTAs let the block scheduler
-    // even out the tail (measured on GB300 against 8-16 KB stages and 3
-    // resident CTAs per SM: 6-10% faster on the four larger workloads).
+    // Stages of ~32 KB and a grid of 48 CTAs per SM, each CTA's ring no
+    // deeper than the groups it gets: where a CTA gets one or two groups
+    // several CTAs are resident per SM, each an independent stream, and the
+    // block scheduler balances them to the end; where CTAs get many groups
+    // one deep ring per SM keeps the bytes in flight.  Chosen on GB300 by
+    // whole-step time (route, plan, permute, combine) over 16-64 KB stages
+    // and 6-64 CTAs per SM: 1-9% faster steps than 6 CTAs per SM on the four
+    // larger workloads.
     const int64_t target = env_int("MOE_PERMUTE_STAGE_BYTES", 32768);
     int64_t G = target / row_bytes;
     if (G < 1) G = 1;
@@ -361,9 +367,9 @@ extern "C" MOE_API int moe_permute(const uint16_t* x, int N, int H, int K, int E
     a.timeout_ns = moe_host::timeout_ns();
     a.early_x = (flags & MOE_PERMUTE_EARLY_X) != 0 ? 1 : 0;
     if (128 + a.slots_bytes + static_cast<size_t>(stages) * a.stage_bytes > kSmemPerSm) return MOE_ERR_UNSUPPORTED;
-    int per_sm = env_int("MOE_PERMUTE_CTAS_PER_SM", 6);
+    int per_sm = env_int("MOE_PERMUTE_CTAS_PER_SM", 48);
     if (per_sm < 1) per_sm = 1;
-    if (per_sm > 16) per_sm = 16;
+    if (per_sm > 64) per_sm = 64;
     int64_t grid = static_cast<int64_t>(moe_host::num_sms()) * per_sm;
     if (grid > a.n_groups) grid = a.n_groups;
     // no deeper ring than the groups a CTA gets: smaller CTAs, more of them resident
