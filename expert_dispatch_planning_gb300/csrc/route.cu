@@ -30,10 +30,10 @@ __device__ __forceinline__ float pow2_int(int n) { return __int_as_float((n + 12
 // exact) and an fp32 tail; e^r by its degree-7 Taylor polynomial (1/j!)
 // in Horner form, one fused multiply-add per step; then 2^n applied as two
 // exact power-of-two factors so intermediate results stay normal.
-__device__ __forceinline__ float exp_nonpos(float t) {
-    if (t != t) return t;
-    if (t > 0.0f) t = 0.0f;
-    if (t < -104.0f) return 0.0f;
+// No branches (lanes of a warp take the same path whatever their t): out of
+// range inputs are clamped for the arithmetic and replaced at the end.
+__device__ __forceinline__ float exp_nonpos(float t_in) {
+    const float t = fmaxf(fminf(t_in, 0.0f), -105.0f);      // NaN -> -105, fixed below
     const float nf = rintf(__fmul_rn(t, 0x1.715476p+0f));  // t / ln2
     float r = __fmaf_rn(-nf, 0x1.62e4p-1f, t);              // - n * ln2 (head)
     r = __fmaf_rn(-nf, 0x1.7f7d1cp-20f, r);                 // - n * ln2 (tail)
@@ -45,22 +45,22 @@ __device__ __forceinline__ float exp_nonpos(float t) {
     p = __fmaf_rn(p, r, 0.5f);
     p = __fmaf_rn(p, r, 1.0f);
     p = __fmaf_rn(p, r, 1.0f);
-    const int n = static_cast<int>(nf);  // -150 <= n <= 0, exact
+    const int n = static_cast<int>(nf);  // -152 <= n <= 0, exact
     const int n1 = n / 2;
     const int n2 = n - n1;
-    return __fmul_rn(__fmul_rn(p, pow2_int(n1)), pow2_int(n2));
+    const float e = __fmul_rn(__fmul_rn(p, pow2_int(n1)), pow2_int(n2));
+    return t_in != t_in ? t_in : (t_in < -104.0f ? 0.0f : e);
 }
 
 // sigmoid(x) = 1 / (1 + e^-x) for x >= 0 and e^x / (1 + e^x) below, each
 // operation rounded once (IEEE division, no flush of subnormals).
+// One path for both signs (numerator selected), so a warp evaluates one
+// exponential and one division per value.
 __device__ __forceinline__ float sigmoid_f32(float x) {
-    if (x != x) return x;
-    if (x >= 0.0f) {
-        const float e = exp_nonpos(-x);
-        return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
-    }
-    const float e = exp_nonpos(x);
-    return __fdiv_rn(e, __fadd_rn(1.0f, e));
+    const bool pos = x >= 0.0f;
+    const float e = exp_nonpos(pos ? -x : x);
+    const float q = __fdiv_rn(pos ? 1.0f : e, __fadd_rn(1.0f, e));
+    return x != x ? x : q;
 }
 
 // Monotone map fp32 -> uint32 (larger float -> larger integer); -0 is
@@ -102,6 +102,32 @@ __device__ __forceinline__ float sigmoid_weight(float x) {
     const float dlo = __fsub_rn(e, __fsub_rn(d, 1.0f));  // exact: 1 + e = d + dlo
     const float q = __fdiv_rn(pos ? 1.0f : e, d);
     return __fmaf_rn(-q, __fdiv_rn(dlo, d), q);
+}
+
+// A lane's two largest keys not yet taken, with their slots and values.
+// Strict comparisons: equal keys keep the lower slot (slots ascend in
+// expert index), as the arg-max tie rule wants.
+template <int V>
+__device__ __forceinline__ void lane_top2(const uint32_t (&key)[V], const float (&raw)[V], uint32_t taken,
+                                          uint32_t& k1, int& j1, float& v1, uint32_t& k2, int& j2, float& v2) {
+    k1 = 0u;
+    k2 = 0u;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const uint32_t kv = ((taken >> v) & 1u) ? 0u : key[v];
+        if (kv > k1) {
+            k2 = k1;
+            j2 = j1;
+            v2 = v1;
+            k1 = kv;
+            j1 = v;
+            v1 = raw[v];
+        } else if (kv > k2) {
+            k2 = kv;
+            j2 = v;
+            v2 = raw[v];
+        }
+    }
 }
 
 struct RouteArgs {
@@ -173,6 +199,13 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_topk_kernel(const RouteAr
 
     const int64_t step = static_cast<int64_t>(gridDim.x) * (ROUTE_THREADS / 32) * TPW;
     int64_t wtok = (static_cast<int64_t>(blockIdx.x) * (ROUTE_THREADS / 32) + warp) * TPW;
+    float bias_r[V];  // this lane's experts' bias, the same for every token
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int e = expert_of<G, V, VEC>(sub, v);
+        bias_r[v] = (sigmoid && a.bias != nullptr && e < E) ? __ldg(a.bias + e) : 0.0f;
+    }
+    const bool has_bias = a.bias != nullptr;
     float nxt[V];
     if (wtok < a.N) load_row<G, V, VEC>(a, wtok + lane / G, sub, nxt);
     for (; wtok < a.N; wtok += step) {
@@ -191,7 +224,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_topk_kernel(const RouteAr
             const int e = expert_of<G, V, VEC>(sub, v);
             if (sigmoid) {
                 const float sg = sigmoid_f32(raw[v]);
-                keyf[v] = a.bias != nullptr && e < E ? __fadd_rn(sg, __ldg(a.bias + e)) : sg;
+                keyf[v] = has_bias ? __fadd_rn(sg, bias_r[v]) : sg;
             } else {
                 keyf[v] = raw[v];
             }
@@ -288,31 +321,63 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_topk_kernel(const RouteAr
             }
         }
 
-        // ---- K rounds of arg-max; each lane keeps its best and rescans only
-        // when its best wins
-        uint32_t bk = 0u, bi = 0xffffffffu;
-        float bv = 0.f;
-#pragma unroll
-        for (int v = 0; v < V; ++v)
-            if (key[v] > bk) {  // values ascend in expert index per lane
-                bk = key[v];
-                bi = static_cast<uint32_t>(expert_of<G, V, VEC>(sub, v));
-                bv = raw[v];
-            }
+        // ---- K rounds of arg-max
         int my_idx[KPL];
         float my_val[KPL];
         float top_val = 0.f;
+        if constexpr (G == 32) {
+            // each lane caches its two best (key, slot, value); a lane whose
+            // cache runs dry rescans its keys minus the ones already taken,
+            // only when it still has some and only then (rare with K <= 8)
+            uint32_t k1 = 0u, k2 = 0u, taken = 0u;
+            int j1 = 0, j2 = 0;
+            float v1 = 0.f, v2 = 0.f;
+            lane_top2<V>(key, raw, taken, k1, j1, v1, k2, j2, v2);
+            int left = 0;  // this lane's eligible keys not yet taken
 #pragma unroll
-        for (int r = 0; r < KMAX; ++r) {
-            if (r >= K) break;
-            uint32_t wi;
-            float wv;
-            if constexpr (G == 32) {
-                const uint32_t m = __reduce_max_sync(FULL_MASK, bk);
-                wi = __reduce_min_sync(FULL_MASK, bk == m ? bi : 0xffffffffu);
+            for (int v = 0; v < V; ++v) left += key[v] != 0u ? 1 : 0;
+            bool dry = false;
+#pragma unroll
+            for (int r = 0; r < KMAX; ++r) {
+                if (r >= K) break;
+                if (__any_sync(FULL_MASK, dry)) {
+                    if (dry) lane_top2<V>(key, raw, taken, k1, j1, v1, k2, j2, v2);
+                    dry = false;
+                }
+                const uint32_t i1 = k1 != 0u ? static_cast<uint32_t>(expert_of<G, V, VEC>(sub, j1)) : 0xffffffffu;
+                const uint32_t m = __reduce_max_sync(FULL_MASK, k1);
+                const uint32_t wi = __reduce_min_sync(FULL_MASK, k1 == m ? i1 : 0xffffffffu);
                 const int owner = VEC ? static_cast<int>((wi / 4) % G) : static_cast<int>(wi % G);
-                wv = __shfl_sync(FULL_MASK, bv, owner);
-            } else {
+                const float wv = __shfl_sync(FULL_MASK, v1, owner);
+                if (i1 == wi) {  // this lane's best won: pop it
+                    taken |= 1u << j1;
+                    --left;
+                    k1 = k2;
+                    j1 = j2;
+                    v1 = v2;
+                    k2 = 0u;
+                    dry = k1 == 0u && left > 0;
+                }
+                if (r == 0) top_val = wv;
+                if (r == sub) {
+                    my_idx[0] = static_cast<int>(wi);
+                    my_val[0] = wv;
+                }
+            }
+        } else {
+            // each lane keeps its best and rescans only when its best wins
+            uint32_t bk = 0u, bi = 0xffffffffu;
+            float bv = 0.f;
+#pragma unroll
+            for (int v = 0; v < V; ++v)
+                if (key[v] > bk) {  // values ascend in expert index per lane
+                    bk = key[v];
+                    bi = static_cast<uint32_t>(expert_of<G, V, VEC>(sub, v));
+                    bv = raw[v];
+                }
+#pragma unroll
+            for (int r = 0; r < KMAX; ++r) {
+                if (r >= K) break;
                 uint32_t ck = bk, ci = bi;
                 float cv = bv;
 #pragma unroll
@@ -326,27 +391,27 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_topk_kernel(const RouteAr
                         cv = ov;
                     }
                 }
-                wi = ci;
-                wv = cv;
-            }
-            if (bi == wi) {  // this lane owned the winner: drop it, find its next best
+                const uint32_t wi = ci;
+                const float wv = cv;
+                if (bi == wi) {  // this lane owned the winner: drop it, find its next best
 #pragma unroll
-                for (int v = 0; v < V; ++v)
-                    if (static_cast<uint32_t>(expert_of<G, V, VEC>(sub, v)) == wi) key[v] = 0u;
-                bk = 0u;
-                bi = 0xffffffffu;
+                    for (int v = 0; v < V; ++v)
+                        if (static_cast<uint32_t>(expert_of<G, V, VEC>(sub, v)) == wi) key[v] = 0u;
+                    bk = 0u;
+                    bi = 0xffffffffu;
 #pragma unroll
-                for (int v = 0; v < V; ++v)
-                    if (key[v] > bk) {
-                        bk = key[v];
-                        bi = static_cast<uint32_t>(expert_of<G, V, VEC>(sub, v));
-                        bv = raw[v];
-                    }
-            }
-            if (r == 0) top_val = wv;
-            if (r % G == sub) {
-                my_idx[r / G] = static_cast<int>(wi);
-                my_val[r / G] = wv;
+                    for (int v = 0; v < V; ++v)
+                        if (key[v] > bk) {
+                            bk = key[v];
+                            bi = static_cast<uint32_t>(expert_of<G, V, VEC>(sub, v));
+                            bv = raw[v];
+                        }
+                }
+                if (r == 0) top_val = wv;
+                if (r % G == sub) {
+                    my_idx[r / G] = static_cast<int>(wi);
+                    my_val[r / G] = wv;
+                }
             }
         }
 
