@@ -149,7 +149,13 @@ def test_plan_configs(m, name, plan_path):
     # small and odd E / R: the shared-memory staging of is_token_in_rank must
     # stay 16-byte aligned for every layout
     (1134, 2, 1, 2, 1, "rand"), (777, 6, 2, 3, 5, "rand"), (333, 3, 3, 1, 2, "rand"),
-    (2000, 10, 3, 5, 7, "rand"), (9001, 2, 2, 1, 4, "rand"), (40000, 6, 1, 2, 3, "rand")])
+    (2000, 10, 3, 5, 7, "rand"), (9001, 2, 2, 1, 4, "rand"), (40000, 6, 1, 2, 3, "rand"),
+    # edges of the one-launch cluster kernels: small-E with 5-bit masks (E = R = 32),
+    # K = 1 and the deepest ring (8 steps, 16 tiles); medium-E just above 32
+    # experts, at 255 / 256 experts, R = 32, K = 32, alignment 1, one token
+    (131072, 32, 1, 32, 4, "rand"), (16384, 32, 2, 32, 16, "hot"), (65536, 8, 1, 8, 2, "rand"),
+    (8192, 33, 2, 3, 5, "rand"), (4096, 255, 5, 5, 7, "dups"), (8192, 256, 8, 32, 128, "rand"),
+    (2048, 192, 32, 16, 3, "dups"), (100, 40, 7, 8, 1, "one"), (1, 33, 1, 1, 1, "rand")])
 def test_plan_shapes(m, N, E, K, R, a, mode, plan_path):
     rng = np.random.default_rng(N + E + K)
     if mode == "one":      # every pair on expert 3: empty experts, one full
