@@ -78,6 +78,8 @@ def algorithmic_bytes(w, P: int) -> dict:
         "route": 4 * N * E + 8 * NK + (4 * E if w.bias else 0),
         "plan_count": 4 * NK,
         "plan_scatter": 4 * NK + 4 * NK + 4 * (NK + E * (w.alignment - 1)) + N * R + 4 * NK,
+        "route_plan_fused": 4 * N * E + 8 * NK + (4 * E if w.bias else 0) + 4 * NK + 4 * NK
+                      + 4 * (NK + E * (w.alignment - 1)) + N * R + 4 * NK,
         "permute": 2 * N * H + 2 * P * H + 4 * NK,
         "combine": 2 * NK * H + 2 * N * H + 8 * NK,
     }
@@ -276,25 +278,15 @@ def run_ours(args, w):
     perm = torch.empty((p.P_cap, w.H), dtype=torch.bfloat16, device=dev)
     out = torch.empty((w.N, w.H), dtype=torch.bfloat16, device=dev)
 
-    def step(ev=None):
-        if ev:
-            ev[0].record(stream)
-        m.route_topk(logits, w.K, topk_idx=idx, topk_w=wts, **rk)
-        if ev:
-            ev[1].record(stream)
-        m.plan(idx, w.E, w.R, w.alignment, out=p)
-        if ev:
-            ev[2].record(stream)
+    def step():
+        # routing and plan in one call (one launch where the sizes allow)
+        m.route_plan(logits, w.K, w.R, w.alignment, topk_idx=idx, topk_w=wts, out=p, **rk)
         m.permute(x, p, out=perm, early_x=True)
-        if ev:
-            ev[3].record(stream)
         m.combine(perm, wts, p, out=out)
-        if ev:
-            ev[4].record(stream)
 
     for _ in range(max(3, args.warmup)):
         step()
-    launches_per_step = 3 + m.plan_launches(w.N, w.E, w.K, w.R)
+    launches_per_step = 2 + m.route_plan_launches(w.N, w.E, w.K, w.R, w.n_group)
     torch.cuda.synchronize()
     status = m.get_status(p)
     if status != 0:
@@ -316,15 +308,24 @@ def run_ours(args, w):
         for name, fn, reps in (("step", step, 1), ("chunk", step, steps_per_graph),
                                ("route", lambda: m.route_topk(logits, w.K, topk_idx=idx, topk_w=wts, **rk), stage_reps),
                                ("plan", lambda: m.plan(idx, w.E, w.R, w.alignment, out=p), stage_reps),
+                               ("route_plan_fused", lambda: m.route_plan(logits, w.K, w.R, w.alignment,
+                                                                         topk_idx=idx, topk_w=wts, out=p, **rk),
+                                stage_reps),
                                # standalone: no overlap with the previous call's tail
                                ("permute", lambda: m.permute(x, p, out=perm), stage_reps),
                                ("combine", lambda: m.combine(perm, wts, p, out=out), stage_reps)):
+            # the one-launch route + plan is opt-in; its graph is captured with it on
+            fused = name == "route_plan_fused"
+            if fused:
+                os.environ["MOE_ROUTE_PLAN_FUSED"] = "1"
             fn()  # warm on the capture stream
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=graph_stream):
                 for _ in range(reps):
                     fn()
             graphs[name] = g
+            if fused:
+                os.environ.pop("MOE_ROUTE_PLAN_FUSED", None)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
@@ -381,7 +382,7 @@ def run_ours(args, w):
         barrier()
         # each kernel alone, same inputs, for its achieved bandwidth
         stage_ms = {k: timed(graphs[k], args.steps) / (args.steps * stage_reps)
-                    for k in ("route", "plan", "permute", "combine")}
+                    for k in ("route", "plan", "route_plan_fused", "permute", "combine")}
     ms = reduce_max(local_ms)
     assert m.get_status(p) == 0
 
@@ -412,8 +413,7 @@ def run_ours(args, w):
             s_cmp.wait_event(ev["in"][b])
             if i >= 2:
                 s_cmp.wait_event(ev["out"][b])       # step i-2's result has left d_out[b]
-            m.route_topk(d_logits[b], w.K, topk_idx=idx, topk_w=wts, **rk)
-            m.plan(idx, w.E, w.R, w.alignment, out=p)
+            m.route_plan(d_logits[b], w.K, w.R, w.alignment, topk_idx=idx, topk_w=wts, out=p, **rk)
             m.permute(d_x[b], p, out=perm, early_x=True)
             ev["used"][b].record(s_cmp)
             m.combine(perm, wts, p, out=d_out[b])
@@ -476,6 +476,7 @@ def run_ours(args, w):
                      "algorithmic_bytes": ab[dom]},
         "kernels": kernels,
         "route_plan_us": round(1e3 * (stage_ms["route"] + stage_ms["plan"]), 2),
+        "route_plan_launches": m.route_plan_launches(w.N, w.E, w.K, w.R, w.n_group),
         "cpu_baseline": cpu,
         "e2e": {"value": ws * w.N / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h_logits[0].numel() * 4 + h_x[0].numel() * 2),

@@ -57,6 +57,9 @@ SIGNATURES = [
                                  _i32, ctypes.c_int32, ctypes.POINTER(MoeBalancedPlanOut), _P]),
     ("moe_tile_map", _i32, [ctypes.POINTER(MoePlanOut), _i32, _i32, _P, _P, _i64, _P, _P]),
     ("moe_rank_layout", _i32, [ctypes.POINTER(MoePlanOut), _i32, _i32, _i32, _P, _P, _P]),
+    ("moe_route_plan", _i32, [_P, _P, _i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_float, _P, _P, _i32, _i32,
+                              _P, ctypes.c_size_t, ctypes.POINTER(MoePlanOut), _P]),
+    ("moe_route_plan_fused", _i32, [_i32, _i32, _i32, _i32, _i32]),
     ("moe_permute", _i32, [_P, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(MoePlanOut), _P, _i32, _P]),
     ("moe_combine", _i32, [_P, _P, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(MoePlanOut), _P, _P]),
     ("moe_get_status", _i32, [ctypes.POINTER(MoePlanOut), ctypes.POINTER(ctypes.c_int32), _P]),

@@ -145,6 +145,41 @@ def plan(topk_idx: torch.Tensor, E: int, R: int, alignment: int, out: Plan | Non
     return out
 
 
+def route_plan(logits: torch.Tensor, K: int, R: int, alignment: int, scoring="softmax", renormalize: bool = True,
+               bias: torch.Tensor | None = None, n_group: int = 1, topk_group: int = 1,
+               routed_scaling: float = 1.0, topk_idx: torch.Tensor | None = None,
+               topk_w: torch.Tensor | None = None, out: Plan | None = None, stream=None):
+    """route_topk then plan in one call (one launch where route_plan_fused says so):
+    returns (topk_idx, topk_w, plan), identical to the two calls."""
+    N, E = logits.shape
+    _need(logits, torch.float32, (N, E), "logits")
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    if topk_idx is None:
+        topk_idx = torch.empty((N, K), dtype=torch.int32, device=logits.device)
+    if topk_w is None:
+        topk_w = torch.empty((N, K), dtype=torch.float32, device=logits.device)
+    _need(topk_idx, torch.int32, (N, K), "topk_idx")
+    _need(topk_w, torch.float32, (N, K), "topk_w")
+    if out is None:
+        out = Plan.allocate(N, E, K, R, alignment, device=logits.device, stream=stream)
+    if (out.N, out.E, out.K, out.R, out.alignment) != (N, E, K, R, alignment):
+        raise ValueError("plan buffers were allocated for other sizes")
+    rc = load().moe_route_plan(_ptr(logits), _ptr(bias), N, E, K, SCORING[scoring], int(bool(renormalize)),
+                               n_group, topk_group, float(routed_scaling), _ptr(topk_idx), _ptr(topk_w), R, alignment,
+                               _ptr(out.workspace), out.workspace.numel(), ctypes.byref(out.c_struct), _stream(stream))
+    check("moe_route_plan", rc)
+    return topk_idx, topk_w, out
+
+
+def route_plan_launches(N: int, E: int, K: int, R: int, n_group: int = 1) -> int:
+    """Kernel launches route_plan makes for these sizes on the current device."""
+    f = int(load().moe_route_plan_fused(N, E, K, R, n_group))
+    if f < 0:
+        raise ValueError("unsupported sizes")
+    return 1 if f == 1 else 1 + plan_launches(N, E, K, R)
+
+
 def plan_launches(N: int, E: int, K: int, R: int) -> int:
     """Kernel launches moe_plan makes for these sizes on the current device."""
     n = int(load().moe_plan_launch_count(N, E, K, R))

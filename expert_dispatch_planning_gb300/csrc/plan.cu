@@ -46,6 +46,7 @@
 #include <tuple>
 
 #include "moe_common.cuh"
+#include "route_core.cuh"
 
 namespace moe {
 
@@ -745,8 +746,81 @@ __device__ __forceinline__ void store_rank_row(uint8_t* row, uint32_t mask, int 
     }
 }
 
-template <int IPT, int NB>
-__global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs a) {
+// Where a warp's expert ids come from.  TopkSource: topk_idx, written by an
+// earlier kernel.  RouteSource: routed here (the fused route + plan), one
+// token per lane with route_token (the router's own arithmetic, so ids and
+// weights are those of the routing kernel), the K winners written to
+// topk_idx / topk_w and handed to the lanes of the (token, k) layout.
+struct TopkSource {
+    template <int IPT>
+    __device__ __forceinline__ void fetch(const PlanArgs& a, int wt0, int lane, int tok_in_iter, int k, int act,
+                                          int (&ids)[IPT]) const {
+#pragma unroll
+        for (int i = 0; i < IPT; ++i) {
+            const int s = wt0 + i * a.tpw + tok_in_iter;
+            ids[i] = (lane < act && s < a.N) ? __ldg(a.topk + s * a.K + k) : -1;
+        }
+    }
+};
+
+constexpr int FUSED_KMAX = 8;  // K <= 8 when routing inside the plan
+
+// V logits per lane (float4 loads), V >= E, E % 4 == 0, K a power of two
+// <= KM (2 or 8: the winners a lane holds), no group limit.  The warp's IPT steps cover IPT * 32 / K tokens,
+// routed 32 at a time (chunk c: tokens wt0 + 32 c + lane); the steps of a
+// chunk take their ids from it with K shuffles.
+template <int V, int KM>
+struct RouteSource {
+    RouteArgs r;
+    template <int IPT>
+    __device__ __forceinline__ void fetch(const PlanArgs& a, int wt0, int lane, int tok_in_iter, int k, int act,
+                                          int (&ids)[IPT]) const {
+        const int K = a.K, tpw = a.tpw;
+        float bias_r[V];
+        lane_bias<1, V, true>(r, 0, bias_r);
+        const int nt = IPT * tpw;  // tokens of this warp
+#pragma unroll
+        for (int i = 0; i < IPT; ++i) ids[i] = -1;
+#pragma unroll
+        for (int c = 0; c < IPT; ++c) {
+            if (c * 32 >= nt) break;
+            const int s = wt0 + c * 32 + lane;
+            const bool valid = c * 32 + lane < nt && s < a.N;
+            float raw[V];
+            load_row<1, V, true>(r, valid ? s : a.N, 0, raw);
+            int widx[KM];
+            float wgt[KM];
+            route_token<1, V, true, KM>(r, raw, bias_r, valid, lane, 0, nullptr, widx, wgt);
+            if (valid) {
+#pragma unroll
+                for (int q = 0; q < KM; ++q)
+                    if (q < K) {
+                        r.topk_idx[static_cast<int64_t>(s) * K + q] = widx[q];
+                        r.topk_w[static_cast<int64_t>(s) * K + q] = wgt[q];
+                    }
+            }
+            // steps i whose tokens lie in this chunk: token i * tpw + tok_in_iter
+            // of the warp sits in lane (i * tpw + tok_in_iter) mod 32
+#pragma unroll
+            for (int i = 0; i < IPT; ++i) {
+                if ((i * tpw) / 32 != c) continue;  // uniform: tpw divides 32
+                const int src = (i * tpw + tok_in_iter) & 31;
+                int id = -1;
+#pragma unroll
+                for (int q = 0; q < KM; ++q) {
+                    if (q >= K) break;
+                    const int v = __shfl_sync(FULL_MASK, widx[q], src);
+                    if (q == k) id = v;
+                }
+                const int st = wt0 + i * tpw + tok_in_iter;
+                ids[i] = (lane < act && st < a.N) ? id : -1;
+            }
+        }
+    }
+};
+
+template <int IPT, int NB, class Src>
+__global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs a, const Src src) {
     constexpr int EP = 1 << NB;         // experts (and ranks) a lane group covers
     constexpr int CHUNKS = 32 / EP;     // lane groups per warp
     constexpr int CW = 2 * EP + 2;      // tile columns: experts, ranks, groups, duplicates
@@ -777,11 +851,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_small_kernel(const PlanArgs
     pdl_wait();
     pdl_trigger();
     int ids[IPT];
-#pragma unroll
-    for (int i = 0; i < IPT; ++i) {
-        const int s = tok0 + (warp * IPT + i) * a.tpw + tok_in_iter;
-        ids[i] = (lane < act && s < a.N) ? __ldg(a.topk + s * K + k) : -1;
-    }
+    src.template fetch<IPT>(a, tok0 + warp * IPT * a.tpw, lane, tok_in_iter, k, act, ids);
 
     // ---- first pass, all in registers
     int cnt_e = 0, cnt_r = 0, run_g = 0, run_d = 0;  // lane x: pairs of expert x / tokens on rank x so far
@@ -1688,11 +1758,11 @@ bool cluster_launchable(Kernel kernel, int T, size_t smem) {
     return ok;
 }
 
-template <typename Kernel>
-int launch_cluster(Kernel kernel, const PlanArgs& a, size_t smem, cudaStream_t stream) {
+template <typename Kernel, typename... Args>
+int launch_cluster(Kernel kernel, int T, size_t smem, cudaStream_t stream, Args... args) {
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = cluster_config(a.T, smem, stream, attr, moe_host::pdl_enabled());
-    return cudaLaunchKernelEx(&cfg, kernel, a) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    cudaLaunchConfig_t cfg = cluster_config(T, smem, stream, attr, moe_host::pdl_enabled());
+    return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 // ---- small-E path geometry: 32 warps per CTA, the fewest warp steps
@@ -1711,6 +1781,22 @@ bool small_geometry(int N, int E, int K, int R, Geom* g) {
         }
     }
     return false;
+}
+
+// Fused route + plan kernels (E <= 8: the logits of a token in two float4;
+// K <= 2 or K <= 8 winners per lane).
+template <int KM, typename F>
+auto with_fused_kernel_k(int ipt, F&& f) {
+    switch (ipt) {
+        case 1: return f(moe::plan_small_kernel<1, 3, moe::RouteSource<8, KM>>, moe::RouteSource<8, KM>{});
+        case 2: return f(moe::plan_small_kernel<2, 3, moe::RouteSource<8, KM>>, moe::RouteSource<8, KM>{});
+        case 4: return f(moe::plan_small_kernel<4, 3, moe::RouteSource<8, KM>>, moe::RouteSource<8, KM>{});
+        default: return f(moe::plan_small_kernel<8, 3, moe::RouteSource<8, KM>>, moe::RouteSource<8, KM>{});
+    }
+}
+template <typename F>
+auto with_fused_kernel(int ipt, int K, F&& f) {
+    return K <= 2 ? with_fused_kernel_k<2>(ipt, f) : with_fused_kernel_k<8>(ipt, f);
 }
 
 // ---- medium-E path geometry: 32 < E <= 256, R <= 32, 32 warps per CTA,
@@ -1758,17 +1844,17 @@ template <typename F>
 auto with_small_kernel(int ipt, int E, F&& f) {
     if (E <= 8) {
         switch (ipt) {
-            case 1: return f(moe::plan_small_kernel<1, 3>);
-            case 2: return f(moe::plan_small_kernel<2, 3>);
-            case 4: return f(moe::plan_small_kernel<4, 3>);
-            default: return f(moe::plan_small_kernel<8, 3>);
+            case 1: return f(moe::plan_small_kernel<1, 3, moe::TopkSource>);
+            case 2: return f(moe::plan_small_kernel<2, 3, moe::TopkSource>);
+            case 4: return f(moe::plan_small_kernel<4, 3, moe::TopkSource>);
+            default: return f(moe::plan_small_kernel<8, 3, moe::TopkSource>);
         }
     }
     switch (ipt) {
-        case 1: return f(moe::plan_small_kernel<1, 5>);
-        case 2: return f(moe::plan_small_kernel<2, 5>);
-        case 4: return f(moe::plan_small_kernel<4, 5>);
-        default: return f(moe::plan_small_kernel<8, 5>);
+        case 1: return f(moe::plan_small_kernel<1, 5, moe::TopkSource>);
+        case 2: return f(moe::plan_small_kernel<2, 5, moe::TopkSource>);
+        case 4: return f(moe::plan_small_kernel<4, 5, moe::TopkSource>);
+        default: return f(moe::plan_small_kernel<8, 5, moe::TopkSource>);
     }
 }
 
@@ -1879,14 +1965,30 @@ int ensure_kernel_attributes() {
             cudaFuncSetAttribute(moe::plan_grid_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, big),
             cudaFuncSetAttribute(moe::plan_grid_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, big),
             cudaFuncSetAttribute(moe::plan_grid_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, big),
-            cudaFuncSetAttribute(moe::plan_small_kernel<1, 3>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
-            cudaFuncSetAttribute(moe::plan_small_kernel<2, 3>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
-            cudaFuncSetAttribute(moe::plan_small_kernel<4, 3>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
-            cudaFuncSetAttribute(moe::plan_small_kernel<8, 3>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
-            cudaFuncSetAttribute(moe::plan_small_kernel<1, 5>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
-            cudaFuncSetAttribute(moe::plan_small_kernel<2, 5>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
-            cudaFuncSetAttribute(moe::plan_small_kernel<4, 5>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
-            cudaFuncSetAttribute(moe::plan_small_kernel<8, 5>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<1, 3, moe::TopkSource>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<2, 3, moe::TopkSource>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<4, 3, moe::TopkSource>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<8, 3, moe::TopkSource>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<1, 5, moe::TopkSource>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<2, 5, moe::TopkSource>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<4, 5, moe::TopkSource>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<8, 5, moe::TopkSource>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<1, 3, moe::RouteSource<8, 2>>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<1, 3, moe::RouteSource<8, 8>>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<2, 3, moe::RouteSource<8, 2>>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<2, 3, moe::RouteSource<8, 8>>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<4, 3, moe::RouteSource<8, 2>>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<4, 3, moe::RouteSource<8, 8>>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<8, 3, moe::RouteSource<8, 2>>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
+            cudaFuncSetAttribute(moe::plan_small_kernel<8, 3, moe::RouteSource<8, 8>>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
             cudaFuncSetAttribute(moe::plan_medium_kernel<1, 4>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
             cudaFuncSetAttribute(moe::plan_medium_kernel<2, 4>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
             cudaFuncSetAttribute(moe::plan_medium_kernel<4, 4>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1),
@@ -1970,9 +2072,12 @@ extern "C" MOE_API int moe_plan_workspace_init(void* workspace, size_t workspace
     return cudaMemsetAsync(workspace, 0, workspace_bytes, stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-extern "C" MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, int R, int alignment,
-                                void* workspace, size_t workspace_bytes, const MoePlanOut* out,
-                                cudaStream_t stream) {
+namespace {
+
+// Host checks of a plan call, and its argument block without the tile
+// geometry and the workspace layout (those depend on the path).
+int plan_args(const int32_t* topk_idx, int N, int E, int K, int R, int alignment, void* workspace,
+              size_t workspace_bytes, const MoePlanOut* out, PlanArgs* a) {
     int rc = check_sizes(N, E, K, R);
     if (rc != MOE_OK) return rc;
     if (alignment < 1 || topk_idx == nullptr || workspace == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
@@ -1985,43 +2090,54 @@ extern "C" MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, in
     for (const void* p : ptrs)
         if (p == nullptr || !aligned(p, 4)) return MOE_ERR_INVALID_ARG;
     if (out->is_token_in_rank == nullptr || !aligned(workspace, 16)) return MOE_ERR_INVALID_ARG;
-
     if (workspace_bytes < plan_ws_bytes(N, E, K, R)) return MOE_ERR_CAPACITY;
     rc = ensure_kernel_attributes();
     if (rc != MOE_OK) return rc;
+
+    a->topk = topk_idx;
+    a->out = *out;
+    a->hdr = static_cast<moe::WsHeader*>(workspace);
+    a->flags = nullptr;
+    a->tile_prefix = nullptr;
+    a->N = N;
+    a->E = E;
+    a->K = K;
+    a->R = R;
+    a->epn = E / R;
+    a->epn_magic = (uint64_t(1) << 32) / static_cast<uint64_t>(a->epn) + 1;
+    a->alignment = alignment;
+    a->p_cap = p_cap;
+    a->skip_tile = moe_host::skip_tile();
+    a->timeout_ns = moe_host::timeout_ns();
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, int R, int alignment,
+                                void* workspace, size_t workspace_bytes, const MoePlanOut* out,
+                                cudaStream_t stream) {
+    PlanArgs a;
+    int rc = plan_args(topk_idx, N, E, K, R, alignment, workspace, workspace_bytes, out, &a);
+    if (rc != MOE_OK) return rc;
     const PathChoice pc = choose_path(N, E, K, R);
     const Geom& g = pc.g;
-
-    PlanArgs a;
-    a.topk = topk_idx;
-    a.out = *out;
-    a.hdr = static_cast<moe::WsHeader*>(workspace);
     a.flags = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) + sizeof(moe::WsHeader));
     a.tile_prefix = reinterpret_cast<int32_t*>(a.flags + static_cast<size_t>(g.T) * (pc.path == PATH_GRID ? 1 : g.C));
-    a.N = N;
-    a.E = E;
-    a.K = K;
-    a.R = R;
-    a.epn = E / R;
-    a.epn_magic = (uint64_t(1) << 32) / static_cast<uint64_t>(a.epn) + 1;
-    a.alignment = alignment;
     a.tpw = g.tpw;
     a.ipt = g.ipt;
     a.tile_tokens = g.tile_tokens;
     a.T = g.T;
     a.C = g.C;
-    a.p_cap = p_cap;
-    a.skip_tile = moe_host::skip_tile();
-    a.timeout_ns = moe_host::timeout_ns();
 
     // ---- one launch: a thread-block cluster of up to 16 tiles, E, R <= 32
     if (pc.path == PATH_SMALL)
-        return with_small_kernel(g.ipt, E, [&](auto kern) { return launch_cluster(kern, a, 0, stream); });
+        return with_small_kernel(g.ipt, E, [&](auto kern) { return launch_cluster(kern, a.T, 0, stream, a, moe::TopkSource{}); });
     // ---- one launch: a thread-block cluster of up to 16 tiles, 32 < E <= 256, R <= 32
     if (pc.path == PATH_MEDIUM)
-        return with_medium_kernel(g.ipt, E, [&](auto kern) { return launch_cluster(kern, a, pc.smem, stream); });
+        return with_medium_kernel(g.ipt, E, [&](auto kern) { return launch_cluster(kern, a.T, pc.smem, stream, a); });
     // ---- one launch: a thread-block cluster of up to 16 tiles, any E
-    if (pc.path == PATH_CLUSTER) return launch_cluster(moe::plan_cluster_kernel, a, pc.smem, stream);
+    if (pc.path == PATH_CLUSTER) return launch_cluster(moe::plan_cluster_kernel, a.T, pc.smem, stream, a);
     // ---- one launch over the whole GPU, all tiles resident at once
     if (pc.path == PATH_GRID) return launch_grid(pc.warps, a, pc.smem, stream);
     // ---- two launches: decoupled look-back over tiles, then the scatter
@@ -2032,6 +2148,55 @@ extern "C" MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, in
     rc = moe_host::launch(moe::plan_count_kernel, dim3(g.T), dim3(moe::PLAN_THREADS), smem1, stream, a);
     if (rc != MOE_OK) return rc;
     return moe_host::launch(moe::plan_scatter_kernel, dim3(g.T), dim3(moe::PLAN_THREADS), smem2, stream, a);
+}
+
+// ---------------------------------------------------------------- fused route + plan
+extern "C" MOE_API int moe_route_plan_fused(int N, int E, int K, int R, int n_group) {
+    if (check_sizes(N, E, K, R) != MOE_OK) return -1;
+    if (ensure_kernel_attributes() != MOE_OK) return -1;
+    // opt-in: on GB300 the fused launch measured slower than the two calls
+    // (routing on the plan's 16 SMs costs what the routing kernel costs on
+    // all of them, whose launch the dependent-launch chain already hides)
+    if (env_int("MOE_ROUTE_PLAN_FUSED", 0) != 1) return 0;
+    const char* env = std::getenv("MOE_PLAN_PATH");
+    if (env != nullptr && std::string(env) != "auto" && std::string(env) != "small") return 0;
+    Geom g;
+    if (n_group != 1 || E > 8 || E % 4 != 0 || K > moe::FUSED_KMAX || (K & (K - 1)) != 0 ||
+        !small_geometry(N, E, K, R, &g))
+        return 0;
+    return with_fused_kernel(g.ipt, K, [&](auto kern, auto) { return cluster_launchable(kern, g.T, 0); }) ? 1 : 0;
+}
+
+extern "C" MOE_API int moe_route_plan(const float* logits, const float* bias, int N, int E, int K, int scoring,
+                                      int renormalize, int n_group, int topk_group, float routed_scaling,
+                                      int32_t* topk_idx, float* topk_w, int R, int alignment, void* workspace,
+                                      size_t workspace_bytes, const MoePlanOut* out, cudaStream_t stream) {
+    const int fused = moe_route_plan_fused(N, E, K, R, n_group);
+    if (fused < 0) return MOE_ERR_INVALID_ARG;
+    if (fused == 0) {  // two calls: the routing kernel, then the plan
+        const int rc = moe_route_topk(logits, bias, N, E, K, scoring, renormalize, n_group, topk_group,
+                                      routed_scaling, topk_idx, topk_w, stream);
+        if (rc != MOE_OK) return rc;
+        return moe_plan(topk_idx, N, E, K, R, alignment, workspace, workspace_bytes, out, stream);
+    }
+    moe::RouteArgs ra;
+    int rc = moe_host::route_args(logits, bias, N, E, K, scoring, renormalize, n_group, topk_group, routed_scaling,
+                                  topk_idx, topk_w, &ra);
+    if (rc != MOE_OK) return rc;
+    PlanArgs a;
+    rc = plan_args(topk_idx, N, E, K, R, alignment, workspace, workspace_bytes, out, &a);
+    if (rc != MOE_OK) return rc;
+    Geom g;
+    small_geometry(N, E, K, R, &g);
+    a.tpw = g.tpw;
+    a.ipt = g.ipt;
+    a.tile_tokens = g.tile_tokens;
+    a.T = g.T;
+    a.C = g.C;
+    return with_fused_kernel(g.ipt, K, [&](auto kern, auto src) {
+        src.r = ra;
+        return launch_cluster(kern, a.T, 0, stream, a, src);
+    });
 }
 
 // ---------------------------------------------------------------- no-allocation variant

@@ -291,6 +291,32 @@ MOE_API int moe_tile_map(const MoePlanOut* plan, int E, int alignment, int32_t* 
 MOE_API int moe_rank_layout(const MoePlanOut* plan, int N, int R, int num_channels,
                             int32_t* channel_prefix_matrix, int32_t* token_rank_slot, cudaStream_t stream);
 
+/*
+ * Routing and the dispatch plan in one call (TensorRT-LLM RoutingKernel.cuh,
+ * routingPermutation, the single-cluster variant that routes and permutes in
+ * one launch below a token count; MoonEP's plan outputs).  Results are those
+ * of moe_route_topk followed by moe_plan with the same arguments, bit for
+ * bit (the kernel runs the router's own arithmetic).  One launch when
+ * moe_route_plan_fused() returns 1 for the sizes, else exactly those two
+ * calls.  Arguments: as for moe_route_topk and moe_plan (topk_idx and
+ * topk_w are written in both cases; the workspace is moe_plan's).
+ */
+MOE_API int moe_route_plan(const float* logits, const float* bias, int N, int E, int K, int scoring,
+                           int renormalize, int n_group, int topk_group, float routed_scaling,
+                           int32_t* topk_idx, float* topk_w, int R, int alignment, void* workspace,
+                           size_t workspace_bytes, const MoePlanOut* out, cudaStream_t stream);
+
+/*
+ * 1 when moe_route_plan runs as one launch for these sizes on the current
+ * device: the environment variable MOE_ROUTE_PLAN_FUSED=1 is set, there is no
+ * group limit (n_group == 1), E <= 8 with E % 4 == 0, K is a power of two
+ * <= 8, R <= 32 and the plan fits one thread-block cluster of up to 16 CTAs;
+ * 0 when it makes the two calls (the default: the one launch measured slower
+ * on GB300, since it routes on the cluster's 16 SMs while the routing kernel
+ * uses all of them); -1 on bad sizes.
+ */
+MOE_API int moe_route_plan_fused(int N, int E, int K, int R, int n_group);
+
 /* ---------------------------------------------------------------- rows */
 /* moe_permute flags. */
 #define MOE_PERMUTE_EARLY_X 1  /* see moe_permute */
