@@ -1648,8 +1648,6 @@ Geom plan_geometry(int N, int E, int K, int R) {
     // size is a function of the sizes alone
     constexpr int64_t kTargetTiles = 152;
     int64_t ipt = (pairs + per_iter * kTargetTiles - 1) / (per_iter * kTargetTiles);
-    const int forced = env_int("MOE_PLAN_IPT", 0);
-    if (forced > 0) ipt = forced;
     if (ipt < 1) ipt = 1;
     if (ipt > moe::PLAN_IPT_MAX) ipt = moe::PLAN_IPT_MAX;
     // shared memory of the scatter kernel: per-pair items, per-warp expert
