@@ -108,8 +108,9 @@ MOE_API int moe_route_topk(const float* logits, const float* bias, int N, int E,
 /*
  * Caller-owned plan outputs (MoonEP MoonEPCommPlan, DeepEP notify_dispatch
  * outputs, in their single-GPU form).  Every pointer is device memory,
- * 4-byte aligned (is_token_in_rank and dst 16-byte aligned).  P denotes the
- * padded row total cu_seqlens[E]; P_cap = moe_plan_capacity_rows(...).
+ * 4-byte aligned (is_token_in_rank may have any alignment; at 16 bytes its
+ * rows are written with vector stores).  P denotes the padded row total
+ * cu_seqlens[E]; P_cap = moe_plan_capacity_rows(...).
  */
 typedef struct MoePlanOut {
     int32_t* tokens_per_expert;  /* [E]     pairs routed to each expert                    */
@@ -180,7 +181,12 @@ MOE_API int moe_plan_workspace_init(void* workspace, size_t workspace_bytes,
  * Slots are canonical: within each expert, pairs keep ascending flat index
  * (MoonEP's stable scatter order), so the plan is a pure function of
  * topk_idx.  Checked here: N >= 1, 1 <= K <= 32, K <= E <= 1024,
- * E % R == 0, R <= 128, N*K < 2^30, P_cap < 2^31.
+ * E % R == 0, R <= 128, N*K < 2^30, P_cap < 2^31.  Recorded in the status
+ * word by the device: MOE_ERR_DEVICE_INDEX (an expert id outside [0, E)),
+ * MOE_ERR_WORKSPACE (a workspace that was never initialised),
+ * MOE_ERR_DEVICE_TIMEOUT (a wait on another tile ran out: 1 s); after an
+ * error the plan's outputs are unspecified and moe_permute / moe_combine
+ * with this plan write nothing.
  */
 MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, int R, int alignment,
                      void* workspace, size_t workspace_bytes, const MoePlanOut* out,
