@@ -64,6 +64,7 @@ SIGNATURES = [
     ("moe_combine", _i32, [_P, _P, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(MoePlanOut), _P, _P]),
     ("moe_get_status", _i32, [ctypes.POINTER(MoePlanOut), ctypes.POINTER(ctypes.c_int32), _P]),
     ("moe_debug_set_plan_fault", _i32, [_i32, _i64]),
+    ("moe_debug_route_sigmoid_error", _i32, [_P, _P]),
 ]
 
 _lock = threading.Lock()

@@ -1,7 +1,15 @@
-// route.cu -- router top-K kernel for one GPU (sm_103a): a grid-stride loop
-// over tokens, G lanes per token, the next token's logits in flight while
-// route_token (route_core.cuh) picks the current token's experts and weights.
-#include "route_core.cuh"
+// route.cu -- router top-K kernels for one GPU (sm_103a).
+//
+// route_topk_kernel: a grid-stride loop over tokens, G lanes per token, the
+// next token's logits in flight while route_token (route_core.cuh) picks the
+// current token's experts and weights; every shape.
+// route_fast_kernel (route_fast.cuh): sigmoid scores over groups of 32
+// experts, selection by approximate keys proved exact, the exact router as
+// the per-token fallback; bit-identical output.
+#include <cstdlib>
+#include <cstring>
+
+#include "route_fast.cuh"
 
 namespace moe {
 
@@ -89,6 +97,48 @@ int dispatch_route(const RouteArgs& a, cudaStream_t stream) {
     return launch_route<32, 32, false, KMAX>(a, stream);
 }
 
+// The selection-by-approximate-keys kernel applies: sigmoid scores, E = 32 G
+// for G in {4, 8, 16}, no groups or one group per 32 experts, K <= G and
+// K <= 8.  MOE_ROUTE_PATH=exact keeps every shape on route_topk_kernel.
+bool route_fast_applies(const RouteArgs& a) {
+    const char* env = std::getenv("MOE_ROUTE_PATH");
+    if (env != nullptr && std::strcmp(env, "exact") == 0) return false;
+    if (a.scoring != MOE_SCORING_SIGMOID || a.E % 32 != 0) return false;
+    const int G = a.E / 32;
+    if (G != 4 && G != 8 && G != 16) return false;
+    if (a.n_group != 1 && a.n_group != G) return false;
+    return a.K <= G && a.K <= 8;
+}
+
+template <int G>
+int launch_route_fast(const RouteArgs& a, cudaStream_t stream) {
+    constexpr int tokens_per_block = moe::RF_WARPS * (32 / G);
+    const int64_t batches = (static_cast<int64_t>(a.N) + tokens_per_block - 1) / tokens_per_block;
+    const size_t smem = sizeof(float) * (32 * G + moe::RF_WARPS * 1024);
+    // one wave of resident blocks, the same number of batches for every block
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, moe::route_fast_kernel<G>, moe::RF_THREADS, smem) !=
+                cudaSuccess || n < 1)
+            n = 1;
+        per_sm = n;
+    }
+    const int64_t cap = static_cast<int64_t>(moe_host::num_sms()) * per_sm;
+    const int64_t rounds = (batches + cap - 1) / cap;
+    const int64_t blocks = (batches + rounds - 1) / rounds;
+    return moe_host::launch(moe::route_fast_kernel<G>, dim3(static_cast<unsigned>(blocks)), dim3(moe::RF_THREADS),
+                            smem, stream, a);
+}
+
+int dispatch_route_fast(const RouteArgs& a, cudaStream_t stream) {
+    switch (a.E / 32) {
+        case 4: return launch_route_fast<4>(a, stream);
+        case 8: return launch_route_fast<8>(a, stream);
+        default: return launch_route_fast<16>(a, stream);
+    }
+}
+
 }  // namespace
 
 extern "C" MOE_API int moe_route_topk(const float* logits, const float* bias, int N, int E, int K,
@@ -99,5 +149,13 @@ extern "C" MOE_API int moe_route_topk(const float* logits, const float* bias, in
     const int rc = moe_host::route_args(logits, bias, N, E, K, scoring, renormalize, n_group, topk_group,
                                         routed_scaling, topk_idx, topk_w, &a);
     if (rc != MOE_OK) return rc;
+    if (route_fast_applies(a)) return dispatch_route_fast(a, stream);
     return K <= 8 ? dispatch_route<8>(a, stream) : dispatch_route<32>(a, stream);
+}
+
+extern "C" MOE_API int moe_debug_route_sigmoid_error(float* max_abs_err, cudaStream_t stream) {
+    if (max_abs_err == nullptr) return MOE_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(max_abs_err, 0, sizeof(float), stream) != cudaSuccess) return MOE_ERR_CUDA;
+    moe::sigmoid_error_kernel<<<moe_host::num_sms() * 8, 256, 0, stream>>>(reinterpret_cast<uint32_t*>(max_abs_err));
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -98,6 +98,17 @@ MOE_API const char* moe_status_string(int code);
  * 1 <= N, 1 <= E <= 1024, E % 4 == 0 for the vector path (any E works).
  * NaN logits are outside the contract (their position in the order is
  * unspecified).
+ *
+ * Sigmoid scores with E = 32*G (G = 4, 8 or 16), n_group 1 or G and
+ * K <= min(G, 8) take a faster kernel with the same output bit for bit: it
+ * chooses candidates by approximate keys (hardware ex2/rcp approximations,
+ * within 2^-20 of the fixed sigmoid for every fp32 input), checks that the
+ * chosen top-K set and kept groups are separated from the rest by more
+ * than twice the keys' error bound, evaluates the fixed sigmoid only for
+ * the winners, and routes any token that fails a check (and every token
+ * when a bias is not finite or exceeds 2^20) with the exact kernel.
+ * MOE_ROUTE_PATH=exact in the environment keeps every call on the exact
+ * kernel.
  */
 MOE_API int moe_route_topk(const float* logits, const float* bias, int N, int E, int K,
                            int scoring, int renormalize, int n_group, int topk_group,
@@ -369,6 +380,14 @@ MOE_API int moe_combine(const uint16_t* y, const float* topk_w, int N, int K, in
  * Returns MOE_ERR_CUDA if the synchronisation or copy fails.
  */
 MOE_API int moe_get_status(const MoePlanOut* plan, int32_t* device_status, cudaStream_t stream);
+
+/*
+ * Self-check of the fast router's error bound: writes to *max_abs_err
+ * (device, one float) the largest |approximate sigmoid - fixed sigmoid|
+ * over every non-NaN fp32 input (2^32 evaluations, a few ms).  The fast
+ * router's margins assume 2^-20.  No counterpart on the pages.
+ */
+MOE_API int moe_debug_route_sigmoid_error(float* max_abs_err, cudaStream_t stream);
 
 /*
  * Test hook for the bounded-wait path: while skip_tile >= 0, the planning
