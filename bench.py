@@ -32,6 +32,8 @@ import workloads  # noqa: E402
 
 METRIC = "routed tokens/s (route+plan+permute+combine)"
 L2_BYTES = 129 * 1024 * 1024
+BALANCED_B = 4             # redundant experts per rank in the balanced-plan timing
+RANK_LAYOUT_CHANNELS = 76  # channels in the rank-layout timing (half the SMs)
 
 
 # ---------------------------------------------------------------- helpers
@@ -82,6 +84,12 @@ def algorithmic_bytes(w, P: int) -> dict:
                       + 4 * (NK + E * (w.alignment - 1)) + N * R + 4 * NK,
         "permute": 2 * N * H + 2 * P * H + 4 * NK,
         "combine": 2 * NK * H + 2 * N * H + 8 * NK,
+        # planning extensions: balanced plan (topk in, dst out, its R x E
+        # matrices), tile map (counts in, two int32 per tile out), rank layout
+        # (is_token_in_rank in; per-(token, rank) slots and the channel matrix out)
+        "balanced": 8 * NK + 4 * (E + R * R + 3 * R * E + 3 * R * (E + BALANCED_B)),
+        "tile_map": 4 * E + 8 * ((NK + E * (w.alignment - 1)) // w.alignment),
+        "rank_layout": N * R + 4 * N * R + 4 * R * RANK_LAYOUT_CHANNELS,
     }
 
 
@@ -507,6 +515,21 @@ def run_stage(args, w):
     p = m.plan(idx, w.E, w.R, w.alignment)
     fns = {"route": lambda: m.route_topk(logits, w.K, topk_idx=idx, topk_w=wts, **rk),
            "plan": lambda: m.plan(idx, w.E, w.R, w.alignment, out=p)}
+    if args.stage == "balanced":
+        # a capacity of 90% of the even share, B redundant experts per rank
+        cap = int(w.N * w.K / w.R * 0.9)
+        nvs = w.N * w.K + (w.E + BALANCED_B) * (w.alignment - 1)
+        bp = m.plan_balanced(idx, p, w.alignment, cap, BALANCED_B, nvs)
+        fns["balanced"] = lambda: m.plan_balanced(idx, p, w.alignment, cap, BALANCED_B, nvs, out=bp)
+    if args.stage == "tile_map":
+        tmax = max(1, p.P_cap // p.alignment)
+        tout = (torch.empty(tmax, dtype=torch.int32, device=dev), torch.empty(tmax, dtype=torch.int32, device=dev),
+                torch.empty(2, dtype=torch.int32, device=dev))
+        fns["tile_map"] = lambda: m.tile_map(p, out=tout)
+    if args.stage == "rank_layout":
+        lws = m.rank_layout_workspace(w.N, w.R)
+        lout = m.rank_layout(p, RANK_LAYOUT_CHANNELS, workspace=lws)
+        fns["rank_layout"] = lambda: m.rank_layout(p, RANK_LAYOUT_CHANNELS, workspace=lws, out=lout)
     if args.stage in ("permute", "combine"):
         x = torch.from_numpy(inp["x_bits"].view(np.int16)).view(torch.bfloat16).to(dev)
         perm = m.permute(x, p)
@@ -551,7 +574,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="mixtral", choices=sorted(workloads.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--stage", choices=["all", "route", "plan", "permute", "combine"], default="all",
+    ap.add_argument("--stage", choices=["all", "route", "plan", "permute", "combine", "balanced", "tile_map",
+                                        "rank_layout"], default="all",
                     help="time one step of the path alone (a profiling case, not a contract line)")
     ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count N")
     args = ap.parse_args(argv)

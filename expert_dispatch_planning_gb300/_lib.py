@@ -56,7 +56,8 @@ SIGNATURES = [
     ("moe_plan_balanced", _i32, [ctypes.POINTER(MoePlanOut), _P, _i32, _i32, _i32, _i32, _i32, ctypes.c_int32,
                                  _i32, ctypes.c_int32, ctypes.POINTER(MoeBalancedPlanOut), _P]),
     ("moe_tile_map", _i32, [ctypes.POINTER(MoePlanOut), _i32, _i32, _P, _P, _i64, _P, _P]),
-    ("moe_rank_layout", _i32, [ctypes.POINTER(MoePlanOut), _i32, _i32, _i32, _P, _P, _P]),
+    ("moe_rank_layout_workspace_size", _size, [_i32, _i32]),
+    ("moe_rank_layout", _i32, [ctypes.POINTER(MoePlanOut), _i32, _i32, _i32, _P, _size, _P, _P, _P]),
     ("moe_route_plan", _i32, [_P, _P, _i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_float, _P, _P, _i32, _i32,
                               _P, ctypes.c_size_t, ctypes.POINTER(MoePlanOut), _P]),
     ("moe_route_plan_fused", _i32, [_i32, _i32, _i32, _i32, _i32]),

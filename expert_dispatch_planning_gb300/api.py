@@ -240,26 +240,45 @@ def plan_balanced(topk_idx: torch.Tensor, p: Plan, token_padding: int, capacity:
     return out
 
 
-def tile_map(p: Plan, max_tiles: int | None = None, stream=None):
+def tile_map(p: Plan, max_tiles: int | None = None, out=None, stream=None):
     """Grouped-GEMM tiles of `p.alignment` rows: (tile_expert, tile_row_limit, sizes[num_tiles, P])."""
-    if max_tiles is None:
-        max_tiles = max(1, p.P_cap // p.alignment)
     dev = p.dst.device
-    te = torch.empty(max_tiles, dtype=torch.int32, device=dev)
-    tl = torch.empty(max_tiles, dtype=torch.int32, device=dev)
-    sizes = torch.empty(2, dtype=torch.int32, device=dev)
+    if out is None:
+        if max_tiles is None:
+            max_tiles = max(1, p.P_cap // p.alignment)
+        out = (torch.empty(max_tiles, dtype=torch.int32, device=dev),
+               torch.empty(max_tiles, dtype=torch.int32, device=dev), torch.empty(2, dtype=torch.int32, device=dev))
+    te, tl, sizes = out
+    max_tiles = te.numel()
+    _need(tl, torch.int32, (max_tiles,), "tile_row_limit")
+    _need(sizes, torch.int32, (2,), "sizes")
     check("moe_tile_map", load().moe_tile_map(ctypes.byref(p.c_struct), p.E, p.alignment, _ptr(te), _ptr(tl),
                                              int(max_tiles), _ptr(sizes), _stream(stream)))
     return te, tl, sizes
 
 
-def rank_layout(p: Plan, num_channels: int, stream=None):
+def rank_layout_workspace(N: int, R: int, device="cuda") -> torch.Tensor:
+    """A workspace for rank_layout of these sizes (reusable across calls)."""
+    n = int(load().moe_rank_layout_workspace_size(N, R))
+    if n == 0:
+        raise ValueError("unsupported rank layout sizes N=%d R=%d" % (N, R))
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def rank_layout(p: Plan, num_channels: int, workspace: torch.Tensor | None = None, out=None, stream=None):
     """(channel_prefix_matrix[R, C], token_rank_slot[N, R]) of a plan."""
     dev = p.dst.device
-    cpm = torch.empty((p.R, num_channels), dtype=torch.int32, device=dev)
-    trs = torch.empty((p.N, p.R), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = rank_layout_workspace(p.N, p.R, device=dev)
+    if out is None:
+        out = (torch.empty((p.R, num_channels), dtype=torch.int32, device=dev),
+               torch.empty((p.N, p.R), dtype=torch.int32, device=dev))
+    cpm, trs = out
+    _need(cpm, torch.int32, (p.R, num_channels), "channel_prefix_matrix")
+    _need(trs, torch.int32, (p.N, p.R), "token_rank_slot")
     check("moe_rank_layout", load().moe_rank_layout(ctypes.byref(p.c_struct), p.N, p.R, int(num_channels),
-                                                   _ptr(cpm), _ptr(trs), _stream(stream)))
+                                                   _ptr(workspace), workspace.numel(), _ptr(cpm), _ptr(trs),
+                                                   _stream(stream)))
     return cpm, trs
 
 

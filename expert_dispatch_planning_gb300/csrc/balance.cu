@@ -6,21 +6,23 @@
 // form: a single source rank, so the prefix over source ranks of tokens per
 // expert is the plain plan's count.
 //
-// Launch 1 (balance_kernel), one CTA of 32 warps, everything in order:
+// Launch 1 (balance_kernel), one CTA of 32 warps, in order:
 //   - warp 0: while some rank is above CAP and some below, move the largest
 //     shortfall from the largest surplus (ties: lower rank); each step zeroes
 //     one rank and a zeroed rank never moves again, so at most R steps;
 //   - one warp per owner rank: hand the owner's expert pairs to its quota
 //     ranks, largest quota and largest remaining expert first (ties: lower
-//     index), then alloc_cumsum by a thread per expert;
-//   - one warp per destination rank: count its remote experts, pick the top
-//     B by pairs (ties to the larger expert index, -1 once no pairs remain),
-//     then a warp scan over its E + B groups for the padded cu_seqlens,
-//     zero-fill ranges and expert offsets.
-// Launch 2 (balance_dst_kernel), a thread per token: each pair's position
-// among its expert's pairs comes from the plain plan (slot - cu[e]); a
-// binary search over alloc_cumsum finds its rank; duplicates by rank as in
-// MoonEP's canonicalisation.
+//     index), then alloc_cumsum by a warp scan per expert.
+//   alloc stays in shared memory when R * (E + 1) is small enough (the large
+//   workload's 64 x 257 is).
+// Launch 2 (balance_groups_kernel), a warp per destination rank: count its
+//   remote experts, pick the top B by pairs (ties to the larger expert
+//   index, -1 once no pairs remain), then a warp scan over its E + B groups
+//   for the padded cu_seqlens, zero-fill ranges and expert offsets.
+// Launch 3 (balance_dst_kernel), a lane per pair: each pair's position
+//   among its expert's pairs comes from the plain plan (slot - cu[e]); a
+//   binary search over alloc_cumsum finds its rank; duplicates by rank as in
+//   MoonEP's canonicalisation.
 #include "moe_common.cuh"
 
 namespace moe {
@@ -38,6 +40,7 @@ struct BalanceArgs {
     MoeBalancedPlanOut out;
     int N, E, K, R, epn, tp, B;
     int32_t cap, NvS;
+    int alloc_in_smem;  // balance_kernel keeps alloc [R][E] in shared memory
 };
 
 // Largest value, lowest index among equals, across the warp (idx >= 0).
@@ -61,6 +64,11 @@ __global__ void __launch_bounds__(BAL_THREADS) balance_kernel(const BalanceArgs 
     int32_t* s_rem = s_bal + R;                // [E] remaining pairs per expert
     int32_t* s_q = s_rem + E;                  // [BAL_WARPS][R] quotas
     int32_t* s_pick = s_q + BAL_WARPS * R;     // [BAL_WARPS][BAL_MAX_B]
+    // alloc [R][E]: in shared memory when it fits (rows padded to E + 1 so a
+    // column read is conflict-free; copied out at the end), else the output
+    // itself; A is a generic pointer to either, AS its row stride
+    int32_t* A = a.alloc_in_smem ? s_pick + BAL_WARPS * BAL_MAX_B : a.out.alloc;
+    const int AS = a.alloc_in_smem ? E + 1 : E;
     __shared__ int s_bad;
 
     pdl_wait();
@@ -72,10 +80,8 @@ __global__ void __launch_bounds__(BAL_THREADS) balance_kernel(const BalanceArgs 
 
     // ---- zero the outputs written sparsely; load counts and balances
     for (int i = tid; i < R * R; i += BAL_THREADS) s_z[i] = 0;
-    for (int i = tid; i < R * E; i += BAL_THREADS) {
-        a.out.alloc[i] = 0;
-        a.out.expert_offsets[i] = 0;
-    }
+    for (int i = tid; i < R * AS; i += BAL_THREADS) A[i] = 0;
+    for (int i = tid; i < R * E; i += BAL_THREADS) a.out.expert_offsets[i] = 0;
     for (int i = tid; i < 2 * R; i += BAL_THREADS) a.out.remote_stats[i] = 0;
     for (int e = tid; e < E; e += BAL_THREADS) s_rem[e] = __ldg(a.counts + e);
     __syncthreads();
@@ -86,19 +92,26 @@ __global__ void __launch_bounds__(BAL_THREADS) balance_kernel(const BalanceArgs 
     }
     __syncthreads();
 
-    // ---- balancing (warp 0): at most R steps
+    // ---- balancing (warp 0, balances in registers: rank lane + 32 q): at
+    // most R steps
     if (warp == 0) {
+        int32_t bv[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) bv[q] = lane + 32 * q < R ? s_bal[lane + 32 * q] : 0;
         for (int step = 0; step <= R; ++step) {
             int32_t hv = INT32_MIN, hi = 0x7fffffff, lv = INT32_MAX, li = 0x7fffffff;
-            for (int r = lane; r < R; r += 32) {
-                const int32_t b = s_bal[r];
-                if (b > hv) {
-                    hv = b;
-                    hi = r;
-                }
-                if (b < lv) {
-                    lv = b;
-                    li = r;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int r = lane + 32 * q;
+                if (r < R) {
+                    if (bv[q] > hv) {
+                        hv = bv[q];
+                        hi = r;
+                    }
+                    if (bv[q] < lv) {
+                        lv = bv[q];
+                        li = r;
+                    }
                 }
             }
             warp_argmax_low(hv, hi);
@@ -108,12 +121,12 @@ __global__ void __launch_bounds__(BAL_THREADS) balance_kernel(const BalanceArgs 
                 if (lane == 0) record_error(a.status, MOE_ERR_DEVICE_INDEX, -1);
                 break;
             }
-            if (lane == 0) {
-                s_bal[hi] -= -lv;
-                s_bal[li] = 0;
-                s_z[hi * R + li] = -lv;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (lane + 32 * q == hi) bv[q] += lv;
+                if (lane + 32 * q == li) bv[q] = 0;
             }
-            __syncwarp();
+            if (lane == 0) s_z[hi * R + li] = -lv;
         }
     }
     __syncthreads();
@@ -145,137 +158,173 @@ __global__ void __launch_bounds__(BAL_THREADS) balance_kernel(const BalanceArgs 
             if (lane == 0) {
                 q[qi] = qv - take;
                 rem[ei] = ev - take;
-                a.out.alloc[static_cast<size_t>(qi) * E + o * epn + ei] = take;
+                A[static_cast<size_t>(qi) * AS + o * epn + ei] = take;
             }
             __syncwarp();
         }
-        for (int le = lane; le < epn; le += 32) a.out.alloc[static_cast<size_t>(o) * E + o * epn + le] = rem[le];
+        for (int le = lane; le < epn; le += 32) A[static_cast<size_t>(o) * AS + o * epn + le] = rem[le];
         __syncwarp();
     }
     __syncthreads();
     for (int i = tid; i < R * R; i += BAL_THREADS) a.out.z[i] = s_z[i];
-    for (int e = tid; e < E; e += BAL_THREADS) {
-        int32_t cum = 0;
-        for (int r = 0; r < R; ++r) {
-            cum += a.out.alloc[static_cast<size_t>(r) * E + e];
-            a.out.alloc_cumsum[static_cast<size_t>(e) * R + r] = cum;
-        }
-    }
-
-    // ---- per destination rank: redundant experts and padded groups
-    for (int d = warp; d < R; d += BAL_WARPS) {
-        const int32_t* row = a.out.alloc + static_cast<size_t>(d) * E;
-        uint32_t cleared = 0u, picked = 0u;  // bit j: expert lane + 32 j (E <= 1024)
-        int nremote = 0;
-        for (int e = lane, j = 0; e < E; e += 32, ++j) {
-            const bool local = e >= d * epn && e < (d + 1) * epn;
-            nremote += (!local && row[e] > 0) ? 1 : 0;
-        }
-        nremote = __reduce_add_sync(FULL_MASK, nremote);
-        if (lane == 0) a.out.remote_stats[2 * d] = nremote;
-        int32_t* picks = s_pick + warp * BAL_MAX_B;
-        for (int slot = 0; slot < B; ++slot) {
-            int32_t bv = 0, bi = -1;
-            for (int e = lane, j = 0; e < E; e += 32, ++j) {
-                const bool local = e >= d * epn && e < (d + 1) * epn;
-                const int32_t c = (local || ((cleared >> j) & 1u)) ? 0 : row[e];
-                if (c >= bv) {  // ties to the larger index
-                    bv = c;
-                    bi = e;
-                }
-            }
-            const int32_t m = __reduce_max_sync(FULL_MASK, bv);
-            const int32_t best = static_cast<int32_t>(__reduce_max_sync(FULL_MASK, bv == m ? bi : -1));
-            const int32_t pick = m > 0 ? best : -1;
-            if (best >= 0 && (best & 31) == lane) {
-                cleared |= 1u << (best >> 5);
-                if (pick >= 0) picked |= 1u << (best >> 5);
-            }
-            if (lane == 0) {
-                picks[slot] = pick;
-                a.out.experts_to_copy[static_cast<size_t>(d) * B + slot] = pick;
-                if (pick >= 0) atomicAdd(a.out.remote_stats + 2 * (pick / epn) + 1, 1);
-            }
-        }
-        __syncwarp();
-        int64_t run = 0;
-        const int G = E + B;
-        for (int g0 = 0; g0 < G; g0 += 32) {
-            const int g = g0 + lane;
-            int32_t c = 0;
-            int expert = -1;
-            if (g < E) {
-                if (!((picked >> (g0 >> 5)) & 1u)) {
-                    c = row[g];
-                    expert = g;
-                }
-            } else if (g < G) {
-                const int32_t sel = picks[g - E];
-                if (sel >= 0) {
-                    c = row[sel];
-                    expert = sel;
-                }
-            }
-            const int64_t padded = c > 0 ? (static_cast<int64_t>(c) + a.tp - 1) / a.tp * a.tp : 0;
-            int64_t incl = padded;
+    if (a.alloc_in_smem)
+        for (int r = warp; r < R; r += BAL_WARPS)
+            for (int e = lane; e < E; e += 32) a.out.alloc[static_cast<size_t>(r) * E + e] = A[static_cast<size_t>(r) * AS + e];
+    // alloc_cumsum [E][R]: a warp per expert scans its column over the ranks
+    // (row-contiguous stores)
+    for (int e = warp; e < E; e += BAL_WARPS) {
+        int32_t run = 0;
+        for (int r0 = 0; r0 < R; r0 += 32) {
+            const int r = r0 + lane;
+            const int32_t v = r < R ? A[static_cast<size_t>(r) * AS + e] : 0;
+            int32_t incl = v;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                const int64_t y = __shfl_up_sync(FULL_MASK, incl, off);
+                const int32_t y = __shfl_up_sync(FULL_MASK, incl, off);
                 if (lane >= off) incl += y;
             }
-            const int64_t base = run + incl - padded;
-            if (g < G) {
-                const size_t gi = static_cast<size_t>(d) * G + g;
-                a.out.rank_cu_seqlens[gi] = static_cast<int32_t>(base + padded);
-                const bool pad = c > 0 && padded > c;
-                a.out.rank_zero_fill[2 * gi] = pad ? static_cast<int32_t>(base + c) : 0;
-                a.out.rank_zero_fill[2 * gi + 1] = pad ? static_cast<int32_t>(padded - c) : 0;
-                if (c > 0) a.out.expert_offsets[static_cast<size_t>(d) * E + expert] = static_cast<int32_t>(base);
-            }
+            if (r < R) a.out.alloc_cumsum[static_cast<size_t>(e) * R + r] = run + incl;
             run += __shfl_sync(FULL_MASK, incl, 31);
         }
-        if (lane == 0 && run > a.NvS) record_error(a.status, MOE_ERR_DEVICE_CAPACITY, d);
     }
+}
+
+// Launch 2 (balance_groups_kernel), a warp per destination rank: its remote
+// experts, the top-B redundant experts by pairs (ties to the larger index,
+// -1 once no pairs remain), then a warp scan over its E + B groups for the
+// padded cu_seqlens, zero-fill ranges and expert offsets.
+constexpr int BAL_GRP_WARPS = 8;
+
+__global__ void __launch_bounds__(BAL_GRP_WARPS * 32) balance_groups_kernel(const BalanceArgs a) {
+    __shared__ int32_t s_pick[BAL_GRP_WARPS][BAL_MAX_B];
+    pdl_wait();
+    pdl_trigger();
+    if (ld_volatile_s32(a.status) != 0) return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int E = a.E, R = a.R, B = a.B, epn = a.epn;
+    const int d = blockIdx.x * BAL_GRP_WARPS + warp;
+    if (d >= R) return;
+    const int32_t* row = a.out.alloc + static_cast<size_t>(d) * E;
+    uint32_t cleared = 0u, picked = 0u;  // bit j: expert lane + 32 j (E <= 1024)
+    int nremote = 0;
+    for (int e = lane, j = 0; e < E; e += 32, ++j) {
+        const bool local = e >= d * epn && e < (d + 1) * epn;
+        nremote += (!local && __ldg(row + e) > 0) ? 1 : 0;
+    }
+    nremote = __reduce_add_sync(FULL_MASK, nremote);
+    if (lane == 0) a.out.remote_stats[2 * d] = nremote;
+    int32_t* picks = s_pick[warp];
+    for (int slot = 0; slot < B; ++slot) {
+        int32_t bv = 0, bi = -1;
+        for (int e = lane, j = 0; e < E; e += 32, ++j) {
+            const bool local = e >= d * epn && e < (d + 1) * epn;
+            const int32_t c = (local || ((cleared >> j) & 1u)) ? 0 : __ldg(row + e);
+            if (c >= bv) {  // ties to the larger index
+                bv = c;
+                bi = e;
+            }
+        }
+        const int32_t m = __reduce_max_sync(FULL_MASK, bv);
+        const int32_t best = static_cast<int32_t>(__reduce_max_sync(FULL_MASK, bv == m ? bi : -1));
+        const int32_t pick = m > 0 ? best : -1;
+        if (best >= 0 && (best & 31) == lane) {
+            cleared |= 1u << (best >> 5);
+            if (pick >= 0) picked |= 1u << (best >> 5);
+        }
+        if (lane == 0) {
+            picks[slot] = pick;
+            a.out.experts_to_copy[static_cast<size_t>(d) * B + slot] = pick;
+            if (pick >= 0) atomicAdd(a.out.remote_stats + 2 * (pick / epn) + 1, 1);
+        }
+    }
+    __syncwarp();
+    int64_t run = 0;
+    const int G = E + B;
+    for (int g0 = 0; g0 < G; g0 += 32) {
+        const int g = g0 + lane;
+        int32_t c = 0;
+        int expert = -1;
+        if (g < E) {
+            if (!((picked >> (g0 >> 5)) & 1u)) {
+                c = __ldg(row + g);
+                expert = g;
+            }
+        } else if (g < G) {
+            const int32_t sel = picks[g - E];
+            if (sel >= 0) {
+                c = __ldg(row + sel);
+                expert = sel;
+            }
+        }
+        const int64_t padded = c > 0 ? (static_cast<int64_t>(c) + a.tp - 1) / a.tp * a.tp : 0;
+        int64_t incl = padded;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int64_t y = __shfl_up_sync(FULL_MASK, incl, off);
+            if (lane >= off) incl += y;
+        }
+        const int64_t base = run + incl - padded;
+        if (g < G) {
+            const size_t gi = static_cast<size_t>(d) * G + g;
+            a.out.rank_cu_seqlens[gi] = static_cast<int32_t>(base + padded);
+            const bool pad = c > 0 && padded > c;
+            a.out.rank_zero_fill[2 * gi] = pad ? static_cast<int32_t>(base + c) : 0;
+            a.out.rank_zero_fill[2 * gi + 1] = pad ? static_cast<int32_t>(padded - c) : 0;
+            if (c > 0) a.out.expert_offsets[static_cast<size_t>(d) * E + expert] = static_cast<int32_t>(base);
+        }
+        run += __shfl_sync(FULL_MASK, incl, 31);
+    }
+    if (lane == 0 && run > a.NvS) record_error(a.status, MOE_ERR_DEVICE_CAPACITY, d);
 }
 
 constexpr int BAL_DST_THREADS = 256;
 
+// A lane per pair: 32 / K tokens per warp, lane (token, k) in k order.  The
+// pair's position among its expert's pairs is slot - cu[e] from the plain
+// plan; the first rank whose allocation prefix exceeds it is its rank; a
+// later k of the same token on the same rank is a duplicate (match.any on
+// (token, rank), the lowest lane is the primary).
 __global__ void __launch_bounds__(BAL_DST_THREADS) balance_dst_kernel(const BalanceArgs a) {
     pdl_wait();
     pdl_trigger();
     if (ld_volatile_s32(a.status) != 0) return;
-    const int64_t s = static_cast<int64_t>(blockIdx.x) * BAL_DST_THREADS + threadIdx.x;
-    if (s >= a.N) return;
+    const int lane = threadIdx.x & 31;
     const int E = a.E, K = a.K, R = a.R;
-    uint32_t seen[4] = {0u, 0u, 0u, 0u};  // R <= 128
-    for (int k = 0; k < K; ++k) {
-        const int64_t f = s * K + k;
+    const int tpw = 32 / K;
+    const int tok_in = lane / K, k = lane - tok_in * K;
+    const int64_t gwarp = (static_cast<int64_t>(blockIdx.x) * BAL_DST_THREADS + threadIdx.x) >> 5;
+    const int64_t s = gwarp * tpw + tok_in;
+    bool ok = tok_in < tpw && s < a.N;
+    const int64_t f = s * K + k;
+    int lo = 0;
+    int32_t d = 0;
+    if (ok) {
         const int e = __ldg(a.topk + f);
         if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
             record_error(a.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(f));
-            return;
+            ok = false;
+        } else {
+            const int32_t gr = raw_slot(__ldg(a.plain_dst + f)) - __ldg(a.cu + e);
+            const int32_t* ac = a.out.alloc_cumsum + static_cast<size_t>(e) * R;
+            int hi = R;  // first rank whose prefix exceeds gr
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (__ldg(ac + mid) > gr)
+                    hi = mid;
+                else
+                    lo = mid + 1;
+            }
+            if (lo >= R || gr < 0) {
+                record_error(a.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(f));
+                ok = false;
+            } else {
+                const int32_t pc = lo > 0 ? __ldg(ac + lo - 1) : 0;
+                d = lo * a.NvS + __ldg(a.out.expert_offsets + static_cast<size_t>(lo) * E + e) + (gr - pc);
+            }
         }
-        const int32_t gr = raw_slot(__ldg(a.plain_dst + f)) - __ldg(a.cu + e);
-        const int32_t* ac = a.out.alloc_cumsum + static_cast<size_t>(e) * R;
-        int lo = 0, hi = R;  // first rank whose prefix exceeds gr
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (__ldg(ac + mid) > gr)
-                hi = mid;
-            else
-                lo = mid + 1;
-        }
-        if (lo >= R || gr < 0) {
-            record_error(a.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(f));
-            return;
-        }
-        const int32_t pc = lo > 0 ? __ldg(ac + lo - 1) : 0;
-        int32_t d = lo * a.NvS + __ldg(a.out.expert_offsets + static_cast<size_t>(lo) * E + e) + (gr - pc);
-        const uint32_t bit = 1u << (lo & 31);
-        if (seen[lo >> 5] & bit) d = -d - 1;
-        seen[lo >> 5] |= bit;
-        a.out.dst[f] = d;
     }
+    const unsigned peers = __match_any_sync(FULL_MASK, ok ? static_cast<unsigned>(tok_in * 128 + lo) : 0xffffffffu);
+    if (ok) a.out.dst[f] = (peers & ((1u << lane) - 1u)) ? -d - 1 : d;
 }
 
 }  // namespace moe
@@ -319,13 +368,20 @@ extern "C" MOE_API int moe_plan_balanced(const MoePlanOut* plan, const int32_t* 
     a.B = B;
     a.cap = capacity;
     a.NvS = NvS;
-    const size_t smem = sizeof(int32_t) * (static_cast<size_t>(R) * R + R + E + static_cast<size_t>(moe::BAL_WARPS) * R +
-                                           static_cast<size_t>(moe::BAL_WARPS) * moe::BAL_MAX_B);
+    size_t smem = sizeof(int32_t) * (static_cast<size_t>(R) * R + R + E + static_cast<size_t>(moe::BAL_WARPS) * R +
+                                     static_cast<size_t>(moe::BAL_WARPS) * moe::BAL_MAX_B);
+    const size_t alloc_bytes = sizeof(int32_t) * static_cast<size_t>(R) * (E + 1);
+    a.alloc_in_smem = smem + alloc_bytes <= 200 * 1024 ? 1 : 0;
+    if (a.alloc_in_smem) smem += alloc_bytes;
     if (cudaFuncSetAttribute(moe::balance_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return MOE_ERR_CUDA;
     int rc = moe_host::launch(moe::balance_kernel, dim3(1), dim3(moe::BAL_THREADS), smem, stream, a);
     if (rc != MOE_OK) return rc;
-    const unsigned blocks = static_cast<unsigned>((N + moe::BAL_DST_THREADS - 1) / moe::BAL_DST_THREADS);
+    rc = moe_host::launch(moe::balance_groups_kernel, dim3((R + moe::BAL_GRP_WARPS - 1) / moe::BAL_GRP_WARPS),
+                          dim3(moe::BAL_GRP_WARPS * 32), 0, stream, a);
+    if (rc != MOE_OK) return rc;
+    const int64_t warps = (static_cast<int64_t>(N) + 32 / K - 1) / (32 / K);
+    const unsigned blocks = static_cast<unsigned>((warps * 32 + moe::BAL_DST_THREADS - 1) / moe::BAL_DST_THREADS);
     return moe_host::launch(moe::balance_dst_kernel, dim3(blocks), dim3(moe::BAL_DST_THREADS), 0, stream, a);
 }

@@ -303,10 +303,17 @@ MOE_API int moe_tile_map(const MoePlanOut* plan, int E, int alignment, int32_t* 
  *                   holds each token once per rank it needs, ranks' blocks
  *                   at rank_prefix[r], tokens in order; -1 if s does not go
  *                   to r.
- * Reads the plan's is_token_in_rank and rank_prefix.  R <= 128.
+ *   workspace       (device) moe_rank_layout_workspace_size(N, R) bytes,
+ *                   256-byte aligned, caller-owned; needs no initialisation
+ *                   (every call rewrites what it reads).  Calls sharing a
+ *                   workspace must not overlap on the GPU.
+ * Reads the plan's is_token_in_rank and rank_prefix.  R <= 128.  Two kernel
+ * launches.  MOE_ERR_CAPACITY if the workspace is too small.
  */
-MOE_API int moe_rank_layout(const MoePlanOut* plan, int N, int R, int num_channels,
-                            int32_t* channel_prefix_matrix, int32_t* token_rank_slot, cudaStream_t stream);
+MOE_API size_t moe_rank_layout_workspace_size(int N, int R);
+MOE_API int moe_rank_layout(const MoePlanOut* plan, int N, int R, int num_channels, void* workspace,
+                            size_t workspace_bytes, int32_t* channel_prefix_matrix, int32_t* token_rank_slot,
+                            cudaStream_t stream);
 
 /*
  * Routing and the dispatch plan in one call (TensorRT-LLM RoutingKernel.cuh,

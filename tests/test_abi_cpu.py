@@ -128,3 +128,22 @@ def test_rows_reject_bad_arguments(lib):
 def test_debug_hook_validates(lib):
     assert lib.moe_debug_set_plan_fault(-2, 0) == 1
     assert lib.moe_debug_set_plan_fault(-1, 0) == 0
+
+
+def test_rank_layout_workspace_and_validation(lib):
+    n = lib.moe_rank_layout_workspace_size(65536, 64)
+    assert n > 0 and n % 4 == 0
+    assert lib.moe_rank_layout_workspace_size(1, 1) > 0
+    assert lib.moe_rank_layout_workspace_size(0, 4) == 0
+    assert lib.moe_rank_layout_workspace_size(16, 129) == 0
+    out = _plan_struct()
+    f = lib.moe_rank_layout
+
+    def call(N=64, R=4, C=3, ws=P(0x10000), ws_bytes=1 << 20, cpm=FAKE, trs=FAKE):
+        return f(ctypes.byref(out), N, R, C, ws, ws_bytes, cpm, trs, None)
+    assert call(C=0) == 1
+    assert call(R=129) == 1
+    assert call(ws=None) == 1
+    assert call(ws=P(0x10010)) == 1                   # 256-byte alignment
+    assert call(ws_bytes=4) == 3                      # too small
+    assert call(trs=None) == 1

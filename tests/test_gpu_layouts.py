@@ -57,3 +57,22 @@ def test_layout_shapes(m, N, E, K, R, a, C):
     cpm, trs = m.rank_layout(p, C)
     o_cpm, o_trs = oracle.rank_layout(want["is_token_in_rank"], C)
     assert np.array_equal(cpm.cpu().numpy(), o_cpm) and np.array_equal(trs.cpu().numpy(), o_trs)
+
+
+def test_rank_layout_workspace_reused_across_sizes_and_calls(m):
+    """One workspace, sized for the largest call, serves smaller calls in a
+    row (no initialisation between them); a too-small one is refused."""
+    from expert_dispatch_planning_gb300 import MoeError
+    ws = m.rank_layout_workspace(9000, 64)
+    for seed, (N, E, K, R, C) in enumerate([(9000, 256, 8, 64, 76), (300, 8, 2, 4, 7), (9000, 64, 4, 16, 1),
+                                            (33, 64, 8, 64, 40)]):
+        rng = np.random.default_rng(seed)
+        topk = workloads.random_topk(rng, N, E, K)
+        p = m.plan(torch.from_numpy(topk).cuda(), E, R, 1)
+        want = oracle.plan(topk, E, R, 1)
+        cpm, trs = m.rank_layout(p, C, workspace=ws)
+        o_cpm, o_trs = oracle.rank_layout(want["is_token_in_rank"], C)
+        assert np.array_equal(cpm.cpu().numpy(), o_cpm) and np.array_equal(trs.cpu().numpy(), o_trs), (N, R, C)
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(MoeError):
+        m.rank_layout(p, 3, workspace=small)
