@@ -3,9 +3,9 @@
 // route_topk_kernel: a grid-stride loop over tokens, G lanes per token, the
 // next token's logits in flight while route_token (route_core.cuh) picks the
 // current token's experts and weights; every shape.
-// route_fast_kernel (route_fast.cuh): sigmoid scores over groups of 32
-// experts, selection by approximate keys proved exact, the exact router as
-// the per-token fallback; bit-identical output.
+// route_fast_kernel (route_fast.cuh): E = 32 G, sigmoid over groups of 32
+// experts or renormalised softmax, selection by approximate keys proved
+// exact, the exact router as the per-token fallback; bit-identical output.
 #include <cstdlib>
 #include <cstring>
 
@@ -97,20 +97,22 @@ int dispatch_route(const RouteArgs& a, cudaStream_t stream) {
     return launch_route<32, 32, false, KMAX>(a, stream);
 }
 
-// The selection-by-approximate-keys kernel applies: sigmoid scores, E = 32 G
-// for G in {4, 8, 16}, no groups or one group per 32 experts, K <= G and
-// K <= 8.  MOE_ROUTE_PATH=exact keeps every shape on route_topk_kernel.
+// The selection-by-approximate-keys kernel applies: E = 32 G for G in
+// {4, 8, 16}, K <= 8, and either sigmoid scores with no groups or one group
+// per 32 experts and K <= G, or renormalised softmax scores without groups.
+// MOE_ROUTE_PATH=exact keeps every shape on route_topk_kernel.
 bool route_fast_applies(const RouteArgs& a) {
     const char* env = std::getenv("MOE_ROUTE_PATH");
     if (env != nullptr && std::strcmp(env, "exact") == 0) return false;
-    if (a.scoring != MOE_SCORING_SIGMOID || a.E % 32 != 0) return false;
+    if (a.E % 32 != 0 || a.K > 8) return false;
     const int G = a.E / 32;
     if (G != 4 && G != 8 && G != 16) return false;
+    if (a.scoring == MOE_SCORING_SOFTMAX) return a.renormalize && a.n_group == 1;
     if (a.n_group != 1 && a.n_group != G) return false;
-    return a.K <= G && a.K <= 8;
+    return a.K <= G;
 }
 
-template <int G>
+template <int G, bool SM>
 int launch_route_fast(const RouteArgs& a, cudaStream_t stream) {
     constexpr int tokens_per_block = moe::RF_WARPS * (32 / G);
     const int64_t batches = (static_cast<int64_t>(a.N) + tokens_per_block - 1) / tokens_per_block;
@@ -119,23 +121,25 @@ int launch_route_fast(const RouteArgs& a, cudaStream_t stream) {
     static int per_sm = 0;
     if (per_sm == 0) {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, moe::route_fast_kernel<G>, moe::RF_THREADS, smem) !=
-                cudaSuccess || n < 1)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, moe::route_fast_kernel<G, SM>, moe::RF_THREADS, smem) !=
+                cudaSuccess ||
+            n < 1)
             n = 1;
         per_sm = n;
     }
     const int64_t cap = static_cast<int64_t>(moe_host::num_sms()) * per_sm;
     const int64_t rounds = (batches + cap - 1) / cap;
     const int64_t blocks = (batches + rounds - 1) / rounds;
-    return moe_host::launch(moe::route_fast_kernel<G>, dim3(static_cast<unsigned>(blocks)), dim3(moe::RF_THREADS),
-                            smem, stream, a);
+    return moe_host::launch(moe::route_fast_kernel<G, SM>, dim3(static_cast<unsigned>(blocks)),
+                            dim3(moe::RF_THREADS), smem, stream, a);
 }
 
+template <bool SM>
 int dispatch_route_fast(const RouteArgs& a, cudaStream_t stream) {
     switch (a.E / 32) {
-        case 4: return launch_route_fast<4>(a, stream);
-        case 8: return launch_route_fast<8>(a, stream);
-        default: return launch_route_fast<16>(a, stream);
+        case 4: return launch_route_fast<4, SM>(a, stream);
+        case 8: return launch_route_fast<8, SM>(a, stream);
+        default: return launch_route_fast<16, SM>(a, stream);
     }
 }
 
@@ -149,7 +153,9 @@ extern "C" MOE_API int moe_route_topk(const float* logits, const float* bias, in
     const int rc = moe_host::route_args(logits, bias, N, E, K, scoring, renormalize, n_group, topk_group,
                                         routed_scaling, topk_idx, topk_w, &a);
     if (rc != MOE_OK) return rc;
-    if (route_fast_applies(a)) return dispatch_route_fast(a, stream);
+    if (route_fast_applies(a))
+        return a.scoring == MOE_SCORING_SOFTMAX ? dispatch_route_fast<true>(a, stream)
+                                                : dispatch_route_fast<false>(a, stream);
     return K <= 8 ? dispatch_route<8>(a, stream) : dispatch_route<32>(a, stream);
 }
 

@@ -1,5 +1,6 @@
-// route_fast.cuh -- the router for sigmoid scores over groups of 32 experts
-// (DeepSeek-style group-limited routing, E = 32 * G), sm_103a.
+// route_fast.cuh -- the router for E = 32 * G experts (G = 4, 8, 16), sm_103a:
+// sigmoid scores over groups of 32 experts (DeepSeek-style group-limited
+// routing) and renormalised softmax scores.
 //
 // The exact router (route_core.cuh) evaluates the fixed-sequence sigmoid for
 // every expert and runs K warp-wide arg-max rounds per token; at E = 256 that
@@ -31,6 +32,11 @@
 //      the exact router's route_token; so is every token when a bias is not
 //      finite or exceeds 2^20 in magnitude.  The margins scale with the
 //      largest |bias| (the keys' ulp).
+//   Softmax: the key is the logit, so a packed key is within 2^-18 of it
+//   (relative); the margins are relative too, and out-of-order winners (a
+//   near-tie inside the top K) go to the exact router.  With 4 lanes per
+//   token a lane holds winners 2*sub and 2*sub + 1, which keeps the
+//   normaliser's summation tree that of the exact router.
 //
 // Logits are staged per warp in shared memory with 16-byte cp.async copies
 // (one 4 KB batch per warp; eight blocks per SM hide the load); each lane reads its 128-byte
@@ -93,12 +99,29 @@ __device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gmem_src
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
+// Separation check of two packed keys hi >= lo.  Sigmoid keys: more than
+// the absolute margin m.  Softmax keys (the logits themselves, approximate
+// only in the 5 replaced low bits, i.e. within 2^-18 relative): more than
+// 2^-16 (|hi| + |lo|) plus room for subnormals.
+template <bool SM>
+__device__ __forceinline__ bool separated(float hi, float lo, float m) {
+    if constexpr (SM) {
+        return __fsub_rn(hi, lo) > __fmaf_rn(0x1p-16f, __fadd_rn(fabsf(hi), fabsf(lo)), 0x1p-120f);
+    } else {
+        return __fsub_rn(hi, lo) > m;
+    }
+}
+
 // One token of the current batch: the segment of G lanes starting at
-// lane t*G.  Returns true when the token needs the exact router.
-template <int G>
+// lane t*G.  SM: softmax scores (key = logit, no groups, renormalised
+// weights); else sigmoid + bias with optional groups of 32.  Lane `sub`
+// holds winners k = KPL*sub + j, j < KPL (KPL = 2 when K > G).  Returns
+// true when the token needs the exact router.
+template <int G, bool SM>
 __device__ __forceinline__ bool route_fast_token(const RouteArgs& a, const float* row, const float* s_bias,
                                                  bool fast_ok, FastMargins mg, int sub, int64_t s, bool valid) {
     constexpr unsigned SEGMASK = G == 32 ? 0xffffffffu : ((1u << G) - 1u);
+    constexpr int KPL = (SM && G < 8) ? 2 : 1;  // winners per lane (K <= 8; sigmoid: K <= G)
     const int lane = threadIdx.x & 31;
     const int segbase = lane & ~(G - 1);
     const int K = a.K;
@@ -115,15 +138,21 @@ __device__ __forceinline__ bool route_fast_token(const RouteArgs& a, const float
     for (int i = 0; i < 8; ++i) {
         const int c = (i + sub) & 7;  // rotated 16-byte chunk: no bank conflicts
         const float4 q = *reinterpret_cast<const float4*>(grp + 4 * c);
-        const float4 bq = *reinterpret_cast<const float4*>(gb + 4 * c);
         const float xs[4] = {q.x, q.y, q.z, q.w};
-        const float bs[4] = {bq.x, bq.y, bq.z, bq.w};
+        float bs[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (!SM) {
+            const float4 bq = *reinterpret_cast<const float4*>(gb + 4 * c);
+            bs[0] = bq.x;
+            bs[1] = bq.y;
+            bs[2] = bq.z;
+            bs[3] = bq.w;
+        }
         const uint32_t jbase = 31u - 4u * static_cast<uint32_t>(c);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const float x = xs[u];
             nan_chk = __fmaf_rn(x, 0.0f, nan_chk);
-            const float ak = __fadd_rn(sigmoid_approx(x), bs[u]);
+            const float ak = SM ? x : __fadd_rn(sigmoid_approx(x), bs[u]);
             float v = __uint_as_float((__float_as_uint(ak) & ~31u) | (jbase - static_cast<uint32_t>(u)));
 #pragma unroll
             for (int d = 0; d < RF_D; ++d) {
@@ -134,10 +163,10 @@ __device__ __forceinline__ bool route_fast_token(const RouteArgs& a, const float
         }
     }
 
-    // ---- 2. group selection
+    // ---- 2. group selection (sigmoid)
     bool kept = true;
     bool fail = !fast_ok || nan_chk != 0.0f;
-    if (a.n_group > 1 && a.topk_group < G) {
+    if (!SM && a.n_group > 1 && a.topk_group < G) {
         const float S = __fadd_rn(L[0], L[1]);
         int rank = 0;
 #pragma unroll
@@ -158,9 +187,11 @@ __device__ __forceinline__ bool route_fast_token(const RouteArgs& a, const float
     }
 
     // ---- 3. K + 1 rounds of arg-max over the kept lanes' heads
-    int my_e = 0;          // winner of round `sub` (sub < K)
+    int my_e[KPL];         // winners k = KPL * sub + j
+#pragma unroll
+    for (int j = 0; j < KPL; ++j) my_e[j] = 0;
     float mK = 0.f, mK1 = 0.f, mprev = 0.f;
-    bool ordered = true;   // consecutive winners separated by the top-K margin
+    bool ordered = true;   // consecutive winners separated by the margin
     int popped = 0;
     bool exhausted = false;
     if (!kept) {
@@ -177,10 +208,10 @@ __device__ __forceinline__ bool route_fast_token(const RouteArgs& a, const float
         const int w = __ffs(eq) - 1;  // lowest lane holding the maximum
         if (r == K - 1) mK = mx;
         if (r == K) mK1 = mx;
-        if (r > 0 && r < K && !(__fsub_rn(mprev, mx) > mg.k)) ordered = false;
+        if (r > 0 && r < K && !separated<SM>(mprev, mx, mg.k)) ordered = false;
         mprev = mx;
         if (r < K) {
-            if (sub == r) my_e = 32 * w + 31 - static_cast<int>(__float_as_uint(mx) & 31u);
+            if (sub == r / KPL) my_e[r % KPL] = 32 * w + 31 - static_cast<int>(__float_as_uint(mx) & 31u);
             if (sub == w) {
 #pragma unroll
                 for (int d = 0; d < RF_D - 1; ++d) L[d] = L[d + 1];
@@ -191,64 +222,89 @@ __device__ __forceinline__ bool route_fast_token(const RouteArgs& a, const float
         }
     }
     if (exhausted) fail = true;
-    if (!(__fsub_rn(mK, mK1) > mg.k)) fail = true;
+    if (!separated<SM>(mK, mK1, mg.k)) fail = true;
+    if (SM && !ordered) fail = true;  // softmax: out-of-order winners go to the exact router
     fail = ((__ballot_sync(FULL_MASK, fail) >> segbase) & SEGMASK) != 0u;
 
     // ---- 4. the winners in exact order.  Consecutive round maxima more
-    // than the margin apart are in exact-key order already (lane k holds
-    // the k-th); otherwise the winners' exact keys sort them (descending,
-    // ties to the lower index) -- for the whole warp when any token needs it.
-    int e = sub < K ? (my_e & (32 * G - 1)) : 0x7fffffff;  // always in range
-    float x = sub < K ? row[e] : 0.f;
-    float xk = x;
-    int ek = e;
-    const bool need_sort = ((__ballot_sync(FULL_MASK, !ordered) >> segbase) & SEGMASK) != 0u;
-    if (__any_sync(FULL_MASK, need_sort)) {
-        uint32_t okey = 0u;
-        if (sub < K) {
-            const float sg = sigmoid_f32(x);
-            okey = order_key(has_bias ? __fadd_rn(sg, s_bias[e]) : sg);
-        }
-        int rank = 0;
+    // than the margin apart are in exact-key order already; otherwise
+    // (sigmoid) the winners' exact keys sort them (descending, ties to the
+    // lower index) -- for the whole warp when any token needs it.
+    int ek[KPL];
+    float xk[KPL];
 #pragma unroll
-        for (int d = 1; d < G; ++d) {
-            const int o = (sub + d) & (G - 1);
-            const uint32_t ko = __shfl_sync(FULL_MASK, okey, o, G);
-            const int eo = __shfl_sync(FULL_MASK, e, o, G);
-            rank += (ko > okey || (ko == okey && eo < e)) ? 1 : 0;
-        }
-        int src = 0;  // the lane whose winner sorts to position `sub`
+    for (int j = 0; j < KPL; ++j) {
+        const bool win = KPL * sub + j < K;
+        ek[j] = win ? (my_e[j] & (32 * G - 1)) : 0x7fffffff;  // always in range
+        xk[j] = win ? row[ek[j] & (32 * G - 1)] : 0.f;
+    }
+    if constexpr (!SM) {
+        const int e = ek[0];
+        const float x = xk[0];
+        const bool need_sort = ((__ballot_sync(FULL_MASK, !ordered) >> segbase) & SEGMASK) != 0u;
+        if (__any_sync(FULL_MASK, need_sort)) {
+            uint32_t okey = 0u;
+            if (sub < K) {
+                const float sg = sigmoid_f32(x);
+                okey = order_key(has_bias ? __fadd_rn(sg, s_bias[e]) : sg);
+            }
+            int rank = 0;
 #pragma unroll
-        for (int d = 0; d < G; ++d) {
-            const int rd = __shfl_sync(FULL_MASK, rank, d, G);
-            if (rd == sub) src = d;
-        }
-        const float xs = __shfl_sync(FULL_MASK, x, src, G);
-        const int es = __shfl_sync(FULL_MASK, e, src, G);
-        if (need_sort) {
-            xk = xs;
-            ek = es;
+            for (int d = 1; d < G; ++d) {
+                const int o = (sub + d) & (G - 1);
+                const uint32_t ko = __shfl_sync(FULL_MASK, okey, o, G);
+                const int eo = __shfl_sync(FULL_MASK, e, o, G);
+                rank += (ko > okey || (ko == okey && eo < e)) ? 1 : 0;
+            }
+            int src = 0;  // the lane whose winner sorts to position `sub`
+#pragma unroll
+            for (int d = 0; d < G; ++d) {
+                const int rd = __shfl_sync(FULL_MASK, rank, d, G);
+                if (rd == sub) src = d;
+            }
+            const float xs = __shfl_sync(FULL_MASK, x, src, G);
+            const int es = __shfl_sync(FULL_MASK, e, src, G);
+            if (need_sort) {
+                xk[0] = xs;
+                ek[0] = es;
+            }
         }
     }
 
-    // the exact router's weight arithmetic, lane k holding winner k
-    float num = 0.f, shi = 0.f, slo = 0.f;
-    if (sub < K) {
-        num = sigmoid_weight(xk);
-        if (a.renormalize && num >= 0x1p-100f) ff_add(shi, slo, num, 0.f);
-    }
-    const bool tiny_tok = ((__ballot_sync(FULL_MASK, sub < K && num < 0x1p-100f) >> segbase) & SEGMASK) != 0u;
-    if (__any_sync(FULL_MASK, tiny_tok)) {
-        double sd = 0.0;
-        if (sub < K) {
-            const double ex = exp(-fabs(static_cast<double>(xk)));
-            sd = xk >= 0.f ? 1.0 / (1.0 + ex) : ex / (1.0 + ex);
-        }
-        double den = sd;
+    // ---- 5. weights with the exact router's arithmetic; with the winners
+    // of lane sub at k = KPL*sub + j, the within-lane sums and the xor
+    // butterfly add in the exact router's tree order
+    float num[KPL], shi = 0.f, slo = 0.f;
+    bool tiny_tok = false;
+    if constexpr (SM) {
+        const float top = __shfl_sync(FULL_MASK, xk[0], 0, G);  // the row maximum
 #pragma unroll
-        for (int off = 1; off < G; off <<= 1) den += __shfl_xor_sync(FULL_MASK, den, off, G);
-        const double scale = a.renormalize ? static_cast<double>(a.scaling) / den : a.scaling;
-        if (tiny_tok) num = static_cast<float>(sd * scale);
+        for (int j = 0; j < KPL; ++j) {
+            num[j] = 0.f;
+            if (KPL * sub + j < K) {
+                num[j] = exp_diff(xk[j], top);
+                ff_add(shi, slo, num[j], 0.f);
+            }
+        }
+    } else {
+        num[0] = 0.f;
+        if (sub < K) {
+            num[0] = sigmoid_weight(xk[0]);
+            if (a.renormalize && num[0] >= 0x1p-100f) ff_add(shi, slo, num[0], 0.f);
+        }
+        tiny_tok = ((__ballot_sync(FULL_MASK, sub < K && num[0] < 0x1p-100f) >> segbase) & SEGMASK) != 0u;
+        if (__any_sync(FULL_MASK, tiny_tok)) {
+            double sd = 0.0;
+            if (sub < K) {
+                const double ex = exp(-fabs(static_cast<double>(xk[0])));
+                sd = xk[0] >= 0.f ? 1.0 / (1.0 + ex) : ex / (1.0 + ex);
+            }
+            double den = sd;
+#pragma unroll
+            for (int off = 1; off < G; off <<= 1) den += __shfl_xor_sync(FULL_MASK, den, off, G);
+            const double scale = a.renormalize ? static_cast<double>(a.scaling) / den : a.scaling;
+            if (tiny_tok) num[0] = static_cast<float>(sd * scale);
+        }
     }
     // (every lane takes part in the shuffles; tokens on the fp64 path keep
     // the value above)
@@ -259,23 +315,31 @@ __device__ __forceinline__ bool route_fast_token(const RouteArgs& a, const float
         ff_add(shi, slo, oh, ol);
     }
     if (!tiny_tok) {
-        if (a.renormalize) {
+        if (SM || a.renormalize) {
             const float q = __fdiv_rn(a.scaling, shi);
             const float qc = __fmaf_rn(-q, __fdiv_rn(slo, shi), q);
-            num = __fmul_rn(num, qc);
+#pragma unroll
+            for (int j = 0; j < KPL; ++j) num[j] = __fmul_rn(num[j], qc);
         } else {
-            num = __fmul_rn(num, a.scaling);
+            num[0] = __fmul_rn(num[0], a.scaling);
         }
     }
-    if (valid && !fail && sub < K) {
-        a.topk_idx[s * K + sub] = ek;
-        a.topk_w[s * K + sub] = num;
+    if (valid && !fail) {
+#pragma unroll
+        for (int j = 0; j < KPL; ++j) {
+            const int k = KPL * sub + j;
+            if (k < K) {
+                a.topk_idx[s * K + k] = ek[j];
+                a.topk_w[s * K + k] = num[j];
+            }
+        }
     }
     return fail;
 }
 
-// G lanes per token (E = 32 G), 32 / G tokens per warp per batch.
-template <int G>
+// G lanes per token (E = 32 G), 32 / G tokens per warp per batch; SM:
+// softmax scores.
+template <int G, bool SM>
 __global__ void __launch_bounds__(RF_THREADS, 8) route_fast_kernel(const RouteArgs a) {
     extern __shared__ __align__(16) float s_mem[];  // bias [E], then [warps][1024] logits
     constexpr int TPW = 32 / G;
@@ -329,7 +393,7 @@ __global__ void __launch_bounds__(RF_THREADS, 8) route_fast_kernel(const RouteAr
         const int64_t s = tok0 + t;
         const bool valid = s < a.N;
         const float* row = cur + t * E;  // rows past N hold stale data; nothing is stored for them
-        const bool fail = route_fast_token<G>(a, row, s_bias, fast_ok, mg, sub, s, valid);
+        const bool fail = route_fast_token<G, SM>(a, row, s_bias, fast_ok, mg, sub, s, valid);
 
         // tokens that failed a check: the exact router, the whole warp on one token
         uint32_t pending = __ballot_sync(FULL_MASK, fail && valid && sub == 0);

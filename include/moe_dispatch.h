@@ -99,10 +99,12 @@ MOE_API const char* moe_status_string(int code);
  * NaN logits are outside the contract (their position in the order is
  * unspecified).
  *
- * Sigmoid scores with E = 32*G (G = 4, 8 or 16), n_group 1 or G and
- * K <= min(G, 8) take a faster kernel with the same output bit for bit: it
- * chooses candidates by approximate keys (hardware ex2/rcp approximations,
- * within 2^-20 of the fixed sigmoid for every fp32 input), checks that the
+ * With E = 32*G (G = 4, 8 or 16) and K <= 8, sigmoid scores with n_group 1
+ * or G and K <= G, and renormalised softmax scores without groups, take a
+ * faster kernel with the same output bit for bit: it chooses candidates by
+ * approximate keys (sigmoid: hardware ex2/rcp approximations, within 2^-20
+ * of the fixed sigmoid for every fp32 input; softmax: the logit with its 5
+ * low bits replaced by the expert's position), checks that the
  * chosen top-K set and kept groups are separated from the rest by more
  * than twice the keys' error bound, evaluates the fixed sigmoid only for
  * the winners, and routes any token that fails a check (and every token

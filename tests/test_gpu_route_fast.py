@@ -1,9 +1,11 @@
 """The router's approximate-key kernel against the exact one.
 
-Sigmoid scores over groups of 32 experts take a kernel that selects by
-hardware-approximated keys and proves the selection exact (margins of twice
-the keys' error bound at the top-K and topk_group boundaries), falling back
-to the exact kernel per token.  Its output must equal the exact kernel's bit
+Sigmoid scores over groups of 32 experts, and renormalised softmax scores,
+at E = 32 G take a kernel that selects by approximate keys (hardware
+approximations of the sigmoid; the logit with 5 low bits replaced for
+softmax) and proves the selection exact (margins of twice the keys' error
+bound at the top-K and topk_group boundaries), falling back to the exact
+kernel per token.  Its output must equal the exact kernel's bit
 for bit, on ordinary rows and on rows built to fail each check (ties,
 near-ties, a group holding most winners, non-finite logits, large biases),
 and match the oracle.  The error bound it assumes is re-measured over every
@@ -41,14 +43,14 @@ def test_sigmoid_approximation_within_half_the_assumed_bound(m):
     assert 0.0 < err <= DELTA_SIGMA / 2, err
 
 
-def route(m, logits, K, bias, monkeypatch, path, **kw):
+def route(m, logits, K, bias, monkeypatch, path, scoring="sigmoid", **kw):
     if path == "exact":
         monkeypatch.setenv("MOE_ROUTE_PATH", "exact")
     else:
         monkeypatch.delenv("MOE_ROUTE_PATH", raising=False)
     lg = torch.from_numpy(logits).cuda()
     b = None if bias is None else torch.from_numpy(bias).cuda()
-    idx, w = m.route_topk(lg, K, scoring="sigmoid", bias=b, **kw)
+    idx, w = m.route_topk(lg, K, scoring=scoring, bias=b, **kw)
     torch.cuda.synchronize()
     monkeypatch.delenv("MOE_ROUTE_PATH", raising=False)
     return idx.cpu().numpy(), w.cpu().numpy()
@@ -145,4 +147,50 @@ def test_fast_near_ties_at_the_boundary(m, monkeypatch):
     assert np.array_equal(fi, ei)
     assert np.array_equal(fw.view(np.uint32), ew.view(np.uint32))
     o_idx, _ = oracle.route_topk(x, 8, scoring=1, bias=bias, **kw)
+    assert np.array_equal(fi, o_idx)
+
+
+SOFTMAX_SHAPES = [(128, 8), (128, 1), (128, 5), (256, 8), (256, 2), (512, 8), (512, 3)]
+
+
+@pytest.mark.parametrize("E,K", SOFTMAX_SHAPES)
+@pytest.mark.parametrize("scale", [1.0, 1e-3, 300.0])
+def test_fast_softmax_equals_exact(m, monkeypatch, E, K, scale):
+    rng = np.random.default_rng(E * 13 + K)
+    G = E // 32
+    x = adversarial_rows(rng, 1001, E, G)
+    x[7::9] = x[7::9] * np.float32(scale)
+    kw = dict(renormalize=True, n_group=1, topk_group=1, routed_scaling=1.5)
+    fi, fw = route(m, x, K, None, monkeypatch, "auto", scoring="softmax", **kw)
+    ei, ew = route(m, x, K, None, monkeypatch, "exact", scoring="softmax", **kw)
+    assert np.array_equal(fi, ei)
+    assert np.array_equal(fw.view(np.uint32), ew.view(np.uint32))
+    fin = np.isfinite(x).all(axis=1)
+    o_idx, o_w = oracle.route_topk(x[fin], K, scoring=0, **kw)
+    assert np.array_equal(fi[fin], o_idx)
+    err = np.abs(fw[fin].astype(np.float64) - o_w)
+    ok = (err <= 1e-6 * np.abs(o_w)) | ((np.abs(o_w) < 2.0 ** -126) & (err <= 2.0 ** -126))
+    assert ok.all()
+
+
+def test_fast_softmax_near_ties_inside_the_top_k(m, monkeypatch):
+    """Winners a few ulps apart (their order decided by the exact keys) and
+    logits that differ only in the packed low bits."""
+    rng = np.random.default_rng(12)
+    N, E = 700, 128
+    x = rng.standard_normal((N, E), dtype=np.float32) - 4.0
+    for s in range(N):
+        base = np.float32(rng.choice([0.5, 1.0, 3.0, -0.75]))
+        experts = rng.choice(E, 12, replace=False)
+        for i, e in enumerate(experts):
+            v = base
+            for _ in range(int(rng.integers(0, 40))):
+                v = np.nextafter(v, np.float32(np.inf))
+            x[s, e] = v
+    kw = dict(renormalize=True, n_group=1, topk_group=1, routed_scaling=1.0)
+    fi, fw = route(m, x, 8, None, monkeypatch, "auto", scoring="softmax", **kw)
+    ei, ew = route(m, x, 8, None, monkeypatch, "exact", scoring="softmax", **kw)
+    assert np.array_equal(fi, ei)
+    assert np.array_equal(fw.view(np.uint32), ew.view(np.uint32))
+    o_idx, _ = oracle.route_topk(x, 8, scoring=0, **kw)
     assert np.array_equal(fi, o_idx)
