@@ -175,6 +175,21 @@ int num_sms();
 int64_t timeout_ns();
 int skip_tile();
 
+// Launch in plain stream order (no programmatic early start): for a kernel
+// whose blocks, started early, would hold shared memory and registers that
+// the running predecessor's later blocks need.
+template <typename Kernel, typename... Args>
+int launch_ordered(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.numAttrs = 0;
+    cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, args...);
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 template <typename Kernel, typename... Args>
 int launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
     cudaLaunchConfig_t cfg = {};

@@ -97,19 +97,32 @@ int dispatch_route(const RouteArgs& a, cudaStream_t stream) {
     return launch_route<32, 32, false, KMAX>(a, stream);
 }
 
-// The selection-by-approximate-keys kernel applies: E = 32 G for G in
+// The selection-by-approximate-keys kernel applies to: E = 32 G for G in
 // {4, 8, 16}, K <= 8, and either sigmoid scores with no groups or one group
 // per 32 experts and K <= G, or renormalised softmax scores without groups.
-// MOE_ROUTE_PATH=exact keeps every shape on route_topk_kernel.
-bool route_fast_applies(const RouteArgs& a) {
-    const char* env = std::getenv("MOE_ROUTE_PATH");
-    if (env != nullptr && std::strcmp(env, "exact") == 0) return false;
+// It runs from 16384 tokens on: below that its own gain (about 1 us at 4096
+// to 8192 tokens) is smaller than what its longer-lived blocks cost the
+// neighbouring plan and row kernels in the route -> plan -> permute ->
+// combine chain (2 to 4 us per step measured at those sizes; at 65536 tokens
+// it saves 80 us).  MOE_ROUTE_PATH=exact keeps every call on
+// route_topk_kernel, MOE_ROUTE_PATH=fast takes the fast kernel at any N.
+bool route_fast_shape(const RouteArgs& a) {
     if (a.E % 32 != 0 || a.K > 8) return false;
     const int G = a.E / 32;
     if (G != 4 && G != 8 && G != 16) return false;
     if (a.scoring == MOE_SCORING_SOFTMAX) return a.renormalize && a.n_group == 1;
     if (a.n_group != 1 && a.n_group != G) return false;
     return a.K <= G;
+}
+
+constexpr int kRouteFastMinTokens = 16384;
+
+bool route_fast_applies(const RouteArgs& a) {
+    const char* env = std::getenv("MOE_ROUTE_PATH");
+    if (env != nullptr && std::strcmp(env, "exact") == 0) return false;
+    if (!route_fast_shape(a)) return false;
+    if (env != nullptr && std::strcmp(env, "fast") == 0) return true;
+    return a.N >= kRouteFastMinTokens;
 }
 
 template <int G, bool SM>
@@ -130,8 +143,10 @@ int launch_route_fast(const RouteArgs& a, cudaStream_t stream) {
     const int64_t cap = static_cast<int64_t>(moe_host::num_sms()) * per_sm;
     const int64_t rounds = (batches + cap - 1) / cap;
     const int64_t blocks = (batches + rounds - 1) / rounds;
-    return moe_host::launch(moe::route_fast_kernel<G, SM>, dim3(static_cast<unsigned>(blocks)),
-                            dim3(moe::RF_THREADS), smem, stream, a);
+    // in stream order: started early, its blocks (17 KB of shared memory
+    // each) slowed the kernel before it by more than the launch gap it hides
+    return moe_host::launch_ordered(moe::route_fast_kernel<G, SM>, dim3(static_cast<unsigned>(blocks)),
+                                    dim3(moe::RF_THREADS), smem, stream, a);
 }
 
 template <bool SM>

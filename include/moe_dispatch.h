@@ -99,9 +99,10 @@ MOE_API const char* moe_status_string(int code);
  * NaN logits are outside the contract (their position in the order is
  * unspecified).
  *
- * With E = 32*G (G = 4, 8 or 16) and K <= 8, sigmoid scores with n_group 1
- * or G and K <= G, and renormalised softmax scores without groups, take a
- * faster kernel with the same output bit for bit: it chooses candidates by
+ * From 16384 tokens on, with E = 32*G (G = 4, 8 or 16) and K <= 8, sigmoid
+ * scores with n_group 1 or G and K <= G, and renormalised softmax scores
+ * without groups, take a faster kernel with the same output bit for bit
+ * (launched in plain stream order): it chooses candidates by
  * approximate keys (sigmoid: hardware ex2/rcp approximations, within 2^-20
  * of the fixed sigmoid for every fp32 input; softmax: the logit with its 5
  * low bits replaced by the expert's position), checks that the
@@ -110,7 +111,7 @@ MOE_API const char* moe_status_string(int code);
  * the winners, and routes any token that fails a check (and every token
  * when a bias is not finite or exceeds 2^20) with the exact kernel.
  * MOE_ROUTE_PATH=exact in the environment keeps every call on the exact
- * kernel.
+ * kernel; MOE_ROUTE_PATH=fast takes the fast one at any token count.
  */
 MOE_API int moe_route_topk(const float* logits, const float* bias, int N, int E, int K,
                            int scoring, int renormalize, int n_group, int topk_group,

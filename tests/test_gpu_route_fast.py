@@ -5,7 +5,8 @@ at E = 32 G take a kernel that selects by approximate keys (hardware
 approximations of the sigmoid; the logit with 5 low bits replaced for
 softmax) and proves the selection exact (margins of twice the keys' error
 bound at the top-K and topk_group boundaries), falling back to the exact
-kernel per token.  Its output must equal the exact kernel's bit
+kernel per token (by default from 16384 tokens on; MOE_ROUTE_PATH=fast
+takes it at any size, as these tests do).  Its output must equal the exact kernel's bit
 for bit, on ordinary rows and on rows built to fail each check (ties,
 near-ties, a group holding most winners, non-finite logits, large biases),
 and match the oracle.  The error bound it assumes is re-measured over every
@@ -44,10 +45,8 @@ def test_sigmoid_approximation_within_half_the_assumed_bound(m):
 
 
 def route(m, logits, K, bias, monkeypatch, path, scoring="sigmoid", **kw):
-    if path == "exact":
-        monkeypatch.setenv("MOE_ROUTE_PATH", "exact")
-    else:
-        monkeypatch.delenv("MOE_ROUTE_PATH", raising=False)
+    # "exact": the exact kernel; otherwise the fast one at any token count
+    monkeypatch.setenv("MOE_ROUTE_PATH", "exact" if path == "exact" else "fast")
     lg = torch.from_numpy(logits).cuda()
     b = None if bias is None else torch.from_numpy(bias).cuda()
     idx, w = m.route_topk(lg, K, scoring=scoring, bias=b, **kw)
