@@ -217,6 +217,8 @@ __device__ __noinline__ void tile_phase1(const PlanArgs& a, int tile, int32_t* s
     const int tok_in_iter = lane / K, k = lane - (lane / K) * K;
     const int tok_lane0 = tok_in_iter * K;
     const unsigned below_tok = (1u << tok_lane0) - 1u;
+    const unsigned tokmask = (K == 32 ? FULL_MASK : ((1u << K) - 1u)) << tok_lane0;  // this token's lanes
+    const int rbits = R > 1 ? 32 - __clz(R - 1) : 0;
     // all of this lane's expert ids first: one memory latency for the tile
     int ids[PLAN_IPT_MAX];
 #pragma unroll
@@ -250,8 +252,15 @@ __device__ __noinline__ void tile_phase1(const PlanArgs& a, int tile, int32_t* s
         __syncwarp();
 
         const int r = active ? rank_of(a, e) : 0;
-        const unsigned key = active ? static_cast<unsigned>(tok_in_iter * 128 + r) : 0xffffffffu;
-        const unsigned pd = __match_any_sync(FULL_MASK, key);
+        // lanes on the same rank: one ballot per bit of the rank (cheaper
+        // than a match.any on a (token, rank) key); pd = this token's pairs
+        // on this lane's rank
+        unsigned pr = __ballot_sync(FULL_MASK, active);
+        for (int b = 0; b < rbits; ++b) {
+            const unsigned rb = __ballot_sync(FULL_MASK, (r >> b) & 1);
+            pr &= ((r >> b) & 1) ? rb : ~rb;
+        }
+        const unsigned pd = active ? (pr & tokmask) : (1u << lane);
         const bool prim = active && (pd & lt) == 0u;
         const bool dup = active && !prim;
         const bool opens = prim && __popc(pd) >= 2;
@@ -278,8 +287,8 @@ __device__ __noinline__ void tile_phase1(const PlanArgs& a, int tile, int32_t* s
         if (s_rtok != nullptr) {
             // tokens per rank: one add per distinct rank of the warp step
             // (per-lane adds on R counters serialise)
-            const unsigned pr = __match_any_sync(FULL_MASK, prim ? r : -1);
-            if (prim && (pr & lt) == 0u) atomicAdd(&s_rtok[r], __popc(pr));
+            const unsigned same = pr & __ballot_sync(FULL_MASK, prim);
+            if (prim && (same & lt) == 0u) atomicAdd(&s_rtok[r], __popc(same));
         }
         s_items[(warp * a.ipt + i) * 32 + lane] =
             active ? pack_item(e, wr, dup, opens, __popc(pd) - 1, opens ? run_g + __popc(gball & lt) : dup_pos, dup_pos)
@@ -448,14 +457,28 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_count_kernel(const PlanArgs
         const unsigned lt = (1u << lane) - 1u;
         const int act = a.tpw * K;
         const int tok_in_iter = lane / K, k = lane - (lane / K) * K;
+        const unsigned tokmask = (K == 32 ? FULL_MASK : ((1u << K) - 1u)) << (tok_in_iter * K);
+        const int rbits = R > 1 ? 32 - __clz(R - 1) : 0;
+        const int64_t tok0 = static_cast<int64_t>(tile) * a.tile_tokens;
+        // all of this lane's expert ids first: one memory latency for the tile
+        int ids[PLAN_IPT_MAX];
+#pragma unroll
+        for (int i = 0; i < PLAN_IPT_MAX; ++i) {
+            const int64_t s = tok0 + static_cast<int64_t>(warp * a.ipt + i) * a.tpw + tok_in_iter;
+            ids[i] = (i < a.ipt && lane < act && s < a.N) ? __ldg(a.topk + s * K + k) : -1;
+        }
         int my_groups = 0, my_dups = 0;
+#pragma unroll 1
         for (int i = 0; i < a.ipt; ++i) {
-            const int64_t s = static_cast<int64_t>(tile) * a.tile_tokens +
-                              static_cast<int64_t>(warp * a.ipt + i) * a.tpw + tok_in_iter;
+            int id = ids[0];
+#pragma unroll
+            for (int q = 1; q < PLAN_IPT_MAX; ++q)
+                if (q == i) id = ids[q];
+            const int64_t s = tok0 + static_cast<int64_t>(warp * a.ipt + i) * a.tpw + tok_in_iter;
             bool active = lane < act && s < a.N;
             int e = E;
             if (active) {
-                e = __ldg(a.topk + s * K + k);
+                e = id;
                 if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
                     record_error(a.out.status, MOE_ERR_DEVICE_INDEX, static_cast<int>(s * K + k));
                     active = false;
@@ -465,13 +488,18 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_count_kernel(const PlanArgs
             const unsigned peers = __match_any_sync(FULL_MASK, e);
             if (active && (peers & lt) == 0u) atomicAdd(&s_tot[e], __popc(peers));
             const int r = active ? rank_of(a, e) : 0;
-            const unsigned key = active ? static_cast<unsigned>(tok_in_iter * 128 + r) : 0xffffffffu;
-            const unsigned pd = __match_any_sync(FULL_MASK, key);
+            // lanes on the same rank: one ballot per bit of the rank
+            unsigned pr = __ballot_sync(FULL_MASK, active);
+            for (int b = 0; b < rbits; ++b) {
+                const unsigned rb = __ballot_sync(FULL_MASK, (r >> b) & 1);
+                pr &= ((r >> b) & 1) ? rb : ~rb;
+            }
+            const unsigned pd = pr & tokmask;  // this token's pairs on this lane's rank
             const bool prim = active && (pd & lt) == 0u;
             if (prim && __popc(pd) >= 2) ++my_groups;
             if (active && !prim) ++my_dups;
-            const unsigned pr = __match_any_sync(FULL_MASK, prim ? r : -1);
-            if (prim && (pr & lt) == 0u) atomicAdd(&s_tot[E + r], __popc(pr));
+            const unsigned same = pr & __ballot_sync(FULL_MASK, prim);  // primaries on this rank
+            if (prim && (same & lt) == 0u) atomicAdd(&s_tot[E + r], __popc(same));
         }
         my_groups = __reduce_add_sync(FULL_MASK, my_groups);
         my_dups = __reduce_add_sync(FULL_MASK, my_dups);
