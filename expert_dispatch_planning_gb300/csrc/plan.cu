@@ -219,6 +219,7 @@ __device__ __noinline__ void tile_phase1(const PlanArgs& a, int tile, int32_t* s
     const unsigned below_tok = (1u << tok_lane0) - 1u;
     const unsigned tokmask = (K == 32 ? FULL_MASK : ((1u << K) - 1u)) << tok_lane0;  // this token's lanes
     const int rbits = R > 1 ? 32 - __clz(R - 1) : 0;
+    const int ebits = E > 1 ? 32 - __clz(E - 1) : 0;
     // all of this lane's expert ids first: one memory latency for the tile
     int ids[PLAN_IPT_MAX];
 #pragma unroll
@@ -244,7 +245,15 @@ __device__ __noinline__ void tile_phase1(const PlanArgs& a, int tile, int32_t* s
                 e = E;
             }
         }
-        const unsigned peers = __match_any_sync(FULL_MASK, e);
+        // lanes with the same expert: one ballot per bit of the expert id
+        // (these passes are latency-bound; a match.any is a long wait)
+        const unsigned amask = __ballot_sync(FULL_MASK, active);
+        unsigned pe = amask;
+        for (int b = 0; b < ebits; ++b) {
+            const unsigned eb = __ballot_sync(FULL_MASK, (e >> b) & 1);
+            pe &= ((e >> b) & 1) ? eb : ~eb;
+        }
+        const unsigned peers = active ? pe : (1u << lane);
         const int base = active ? s_wc[warp * E + e] : 0;
         const int wr = base + __popc(peers & lt);
         __syncwarp();
@@ -255,7 +264,7 @@ __device__ __noinline__ void tile_phase1(const PlanArgs& a, int tile, int32_t* s
         // lanes on the same rank: one ballot per bit of the rank (cheaper
         // than a match.any on a (token, rank) key); pd = this token's pairs
         // on this lane's rank
-        unsigned pr = __ballot_sync(FULL_MASK, active);
+        unsigned pr = amask;
         for (int b = 0; b < rbits; ++b) {
             const unsigned rb = __ballot_sync(FULL_MASK, (r >> b) & 1);
             pr &= ((r >> b) & 1) ? rb : ~rb;
@@ -459,6 +468,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_count_kernel(const PlanArgs
         const int tok_in_iter = lane / K, k = lane - (lane / K) * K;
         const unsigned tokmask = (K == 32 ? FULL_MASK : ((1u << K) - 1u)) << (tok_in_iter * K);
         const int rbits = R > 1 ? 32 - __clz(R - 1) : 0;
+        const int ebits = E > 1 ? 32 - __clz(E - 1) : 0;
         const int64_t tok0 = static_cast<int64_t>(tile) * a.tile_tokens;
         // all of this lane's expert ids first: one memory latency for the tile
         int ids[PLAN_IPT_MAX];
@@ -485,11 +495,17 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_count_kernel(const PlanArgs
                     e = E;
                 }
             }
-            const unsigned peers = __match_any_sync(FULL_MASK, e);
+            // lanes with the same expert, then on the same rank: one ballot
+            // per bit of the id
+            const unsigned amask = __ballot_sync(FULL_MASK, active);
+            unsigned peers = amask;
+            for (int b = 0; b < ebits; ++b) {
+                const unsigned eb = __ballot_sync(FULL_MASK, (e >> b) & 1);
+                peers &= ((e >> b) & 1) ? eb : ~eb;
+            }
             if (active && (peers & lt) == 0u) atomicAdd(&s_tot[e], __popc(peers));
             const int r = active ? rank_of(a, e) : 0;
-            // lanes on the same rank: one ballot per bit of the rank
-            unsigned pr = __ballot_sync(FULL_MASK, active);
+            unsigned pr = amask;
             for (int b = 0; b < rbits; ++b) {
                 const unsigned rb = __ballot_sync(FULL_MASK, (r >> b) & 1);
                 pr &= ((r >> b) & 1) ? rb : ~rb;
@@ -1578,14 +1594,16 @@ __global__ void __launch_bounds__(WARPS * 32) plan_grid_kernel(const PlanArgs a)
 
     // ---- publish: counts, then the flag (every writer fences before the
     // barrier, so the flag store is ordered after all of them)
-    int32_t* counts = a.tile_prefix;  // [C][T]
-    for (int c = tid; c < C; c += THREADS) {
-        st_relaxed_s32(counts + static_cast<size_t>(c) * T + tile, s_cnt[c]);
-        __threadfence();
-    }
+    int32_t* counts = a.tile_prefix;  // [C][T], T padded to a multiple of 4
+    const int TP = (T + 3) & ~3;
+    for (int c = tid; c < C; c += THREADS) st_relaxed_s32(counts + static_cast<size_t>(c) * TP + tile, s_cnt[c]);
     __syncthreads();
-    if (tid == 0 && tile != a.skip_tile)
+    // one fence after the barrier orders every thread's count stores (the
+    // barrier makes them observed by thread 0; fences are cumulative)
+    if (tid == 0 && tile != a.skip_tile) {
+        __threadfence();
         st_relaxed_u64(a.flags + tile, pack_flag(epoch, s_bad ? ST_ERR : ST_PRE, 0u));
+    }
 
     // ---- wait for every tile's flag (a thread per tile; T <= THREADS)
     if (tid < T) {
@@ -1615,12 +1633,20 @@ __global__ void __launch_bounds__(WARPS * 32) plan_grid_kernel(const PlanArgs a)
         // the per-rank columns are needed by tile 0 only
         for (int c = warp; c < C; c += WARPS) {
             if (tile != 0 && c >= E && c < E + R) continue;
-            const int32_t* col = counts + static_cast<size_t>(c) * T;
+            const int32_t* col = counts + static_cast<size_t>(c) * TP;
             int32_t tot = 0, ex = 0;
-            for (int j = lane; j < T; j += 32) {
-                const int32_t v = ld_relaxed_s32(col + j);
-                tot += v;
-                ex += j < tile ? v : 0;
+            // 16-byte loads at L2 (past L1, written by other SMs): one
+            // round trip per column for T <= 128
+            for (int j = 4 * lane; j < T; j += 128) {
+                const int4 v = __ldcg(reinterpret_cast<const int4*>(col + j));
+                const int32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (j + u < T) {
+                        tot += x[u];
+                        ex += j + u < tile ? x[u] : 0;
+                    }
+                }
             }
             tot = __reduce_add_sync(FULL_MASK, tot);
             ex = __reduce_add_sync(FULL_MASK, ex);
@@ -1701,7 +1727,7 @@ Geom plan_geometry(int N, int E, int K, int R) {
 
 size_t ws_bytes(const Geom& g) {
     size_t b = sizeof(moe::WsHeader);
-    b += sizeof(uint64_t) * static_cast<size_t>(g.T) * g.C;
+    b += sizeof(uint64_t) * static_cast<size_t>(g.T) * g.C + 8;  // + 16-byte alignment of tile_prefix
     b += sizeof(int32_t) * static_cast<size_t>(g.T) * g.C;
     return (b + 15) / 16 * 16;
 }
@@ -1925,8 +1951,8 @@ bool grid_geometry(int N, int E, int K, int R, Geom* g, int* warps) {
 
 // header, then flags u64[T], then counts i32[C][T]
 size_t grid_ws_bytes(const Geom& g) {
-    const size_t b = sizeof(moe::WsHeader) + sizeof(uint64_t) * static_cast<size_t>(g.T) +
-                     sizeof(int32_t) * static_cast<size_t>(g.T) * g.C;
+    const size_t b = sizeof(moe::WsHeader) + sizeof(uint64_t) * static_cast<size_t>(g.T) + 8 +
+                     sizeof(int32_t) * static_cast<size_t>((g.T + 3) & ~3) * g.C;
     return (b + 15) / 16 * 16;
 }
 
@@ -2149,7 +2175,12 @@ extern "C" MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, in
     const PathChoice pc = choose_path(N, E, K, R);
     const Geom& g = pc.g;
     a.flags = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) + sizeof(moe::WsHeader));
-    a.tile_prefix = reinterpret_cast<int32_t*>(a.flags + static_cast<size_t>(g.T) * (pc.path == PATH_GRID ? 1 : g.C));
+    {
+        // the grid path reads its counts with 16-byte loads: start them on a
+        // 16-byte boundary (the workspace itself is 16-byte aligned)
+        const uintptr_t p = reinterpret_cast<uintptr_t>(a.flags + static_cast<size_t>(g.T) * (pc.path == PATH_GRID ? 1 : g.C));
+        a.tile_prefix = reinterpret_cast<int32_t*>((p + 15) & ~static_cast<uintptr_t>(15));
+    }
     a.tpw = g.tpw;
     a.ipt = g.ipt;
     a.tile_tokens = g.tile_tokens;
