@@ -10,11 +10,11 @@
 //
 //   1. G lanes per token, lane `sub` owns the 32 contiguous experts of group
 //      `sub`.  Approximate key a = rcp.approx(1 + ex2.approx(-x log2 e)) + b,
-//      within DELTA_SIGMA (checked over every fp32 input by
-//      moe_debug_route_sigmoid_error) plus one key rounding of the exact key.
-//      The expert's lane-local index is packed into the 5 low bits of a, so
-//      that packed keys are distinct within a lane; a 6-deep min/max network
-//      keeps the lane's six largest.
+//      within RF_DELTA_SIGMA of the fixed sigmoid (re-measured over every
+//      fp32 input by moe_debug_route_sigmoid_error) plus one key rounding of
+//      the exact key.  The expert's lane-local index is packed into the 5
+//      low bits of a, so that packed keys are distinct within a lane; a
+//      6-deep min/max network keeps the lane's six largest.
 //   2. Group score = sum of the lane's two largest packed keys; the
 //      topk_group best groups (rank by shuffles within the token) are kept.
 //   3. K + 1 rounds of arg-max over the kept lanes' list heads (max by xor
@@ -23,10 +23,12 @@
 //      by more than twice the packed keys' error bound.  Then no exact key
 //      can reorder across either boundary, and the exact top-K set and the
 //      exact kept groups are the approximate ones.
-//   4. The K winners' exact keys (same fixed sigmoid as the exact router)
-//      sort them (descending, ties to the lower index), and the weights are
-//      computed in sorted position with the exact router's arithmetic and
-//      summation order, so the output is bit-identical to it.
+//   4. Winners whose consecutive round maxima are separated by the same
+//      margin are already in exact order; otherwise (sigmoid) their exact
+//      keys (the exact router's fixed sigmoid) sort them, descending, ties
+//      to the lower index.  The weights are computed in sorted position with
+//      the exact router's arithmetic and summation order, so the output is
+//      bit-identical to it.
 //   5. A token that fails a check (a margin, a lane that ran out of its six
 //      candidates, a NaN or infinite logit) is routed by the whole warp with
 //      the exact router's route_token; so is every token when a bias is not
@@ -39,9 +41,9 @@
 //   normaliser's summation tree that of the exact router.
 //
 // Logits are staged per warp in shared memory with 16-byte cp.async copies
-// (one 4 KB batch per warp; eight blocks per SM hide the load); each lane reads its 128-byte
-// group with a rotated chunk order so that the eight lanes of a token hit
-// eight different bank quads.
+// (one 4 KB batch per warp; eight blocks per SM hide the load); each lane
+// reads its 128-byte group in a rotated chunk order so that the eight lanes
+// of a token hit eight different bank quads.
 #pragma once
 
 #include "route_core.cuh"
