@@ -177,6 +177,8 @@ def route_plan_launches(N: int, E: int, K: int, R: int, n_group: int = 1) -> int
     f = int(load().moe_route_plan_fused(N, E, K, R, n_group))
     if f < 0:
         raise ValueError("unsupported sizes")
+    if N == 0:      # nothing to route: the plan's launch alone
+        return plan_launches(N, E, K, R)
     return 1 if f == 1 else 1 + plan_launches(N, E, K, R)
 
 

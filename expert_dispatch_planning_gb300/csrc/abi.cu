@@ -79,7 +79,7 @@ extern "C" MOE_API int moe_debug_set_plan_fault(int skip_tile, int64_t timeout_n
 // set of buffers of the same sizes, one asynchronous device copy per array.
 extern "C" MOE_API int moe_plan_copy(const MoePlanOut* src, const MoePlanOut* dst, int N, int E, int K, int R,
                                      int alignment, cudaStream_t stream) {
-    if (src == nullptr || dst == nullptr || N < 1 || E < 1 || K < 1 || R < 1 || alignment < 1 || E % R != 0)
+    if (src == nullptr || dst == nullptr || N < 0 || E < 1 || K < 1 || R < 1 || alignment < 1 || E % R != 0)
         return MOE_ERR_INVALID_ARG;
     const int64_t p_cap = moe_plan_capacity_rows(N, E, K, alignment);
     if (p_cap < 0) return MOE_ERR_INVALID_ARG;

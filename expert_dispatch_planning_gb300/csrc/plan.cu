@@ -1677,6 +1677,37 @@ __global__ void __launch_bounds__(WARPS * 32) plan_grid_kernel(const PlanArgs a)
     }
 }
 
+// ---------------------------------------------------------------- empty batch
+// N = 0 (a batch with no tokens): every count, offset and prefix is zero,
+// no expert has padding, and every row of the capacity E * (alignment - 1)
+// is unused (-1).  The arrays sized by N have no elements.
+__global__ void __launch_bounds__(256) plan_empty_kernel(const MoePlanOut out, int E, int R, int64_t p_cap) {
+    pdl_wait();
+    pdl_trigger();
+    if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+            out.cu_seqlens[i] = 0;
+            if (i < E) {
+                out.tokens_per_expert[i] = 0;
+                out.zero_fill_ranges[2 * i] = 0;
+                out.zero_fill_ranges[2 * i + 1] = 0;
+            }
+        }
+        for (int i = threadIdx.x; i <= R; i += blockDim.x) {
+            out.rank_prefix[i] = 0;
+            out.rank_slot_offsets[i] = 0;
+            if (i < R) {
+                out.pairs_per_rank[i] = 0;
+                out.tokens_per_rank[i] = 0;
+            }
+        }
+        if (threadIdx.x < 2) out.dup_counts[threadIdx.x] = 0;
+    }
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < p_cap; j += stride)
+        out.src_of_slot[j] = -1;
+}
+
 }  // namespace moe
 
 // ---------------------------------------------------------------- host
@@ -1734,8 +1765,9 @@ size_t ws_bytes(const Geom& g) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// N = 0 is a valid, empty batch.
 int check_sizes(int N, int E, int K, int R) {
-    if (N < 1 || E < 1 || E > 1024 || K < 1 || K > 32 || K > E || R < 1 || R > 128 || E % R != 0)
+    if (N < 0 || E < 1 || E > 1024 || K < 1 || K > 32 || K > E || R < 1 || R > 128 || E % R != 0)
         return MOE_ERR_INVALID_ARG;
     if (static_cast<int64_t>(N) * K >= (int64_t(1) << 30)) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
@@ -1958,6 +1990,7 @@ size_t grid_ws_bytes(const Geom& g) {
 
 // Workspace for every path the sizes allow.
 size_t plan_ws_bytes(int N, int E, int K, int R) {
+    if (N == 0) return sizeof(moe::WsHeader);  // the empty plan reads no workspace
     size_t b = ws_bytes(plan_geometry(N, E, K, R));
     Geom gg;
     int w = 0;
@@ -2103,7 +2136,7 @@ PathChoice choose_path(int N, int E, int K, int R) {
 }  // namespace
 
 extern "C" MOE_API int64_t moe_plan_capacity_rows(int N, int E, int K, int alignment) {
-    if (N < 1 || E < 1 || K < 1 || alignment < 1) return -1;
+    if (N < 0 || E < 1 || K < 1 || alignment < 1) return -1;
     return static_cast<int64_t>(N) * K + static_cast<int64_t>(E) * (alignment - 1);
 }
 
@@ -2114,6 +2147,7 @@ extern "C" MOE_API size_t moe_plan_workspace_size(int N, int E, int K, int R) {
 
 extern "C" MOE_API int moe_plan_launch_count(int N, int E, int K, int R) {
     if (check_sizes(N, E, K, R) != MOE_OK) return -1;
+    if (N == 0) return 1;  // plan_empty_kernel
     if (ensure_kernel_attributes() != MOE_OK) return -1;
     return choose_path(N, E, K, R).path == PATH_LOOKBACK ? 2 : 1;
 }
@@ -2166,9 +2200,37 @@ int plan_args(const int32_t* topk_idx, int N, int E, int K, int R, int alignment
 
 }  // namespace
 
+namespace {
+
+// The plan of an empty batch (N = 0): one small launch that writes the
+// E- and R-sized outputs and marks the capacity rows unused.  topk_idx, the
+// workspace and the N-sized arrays (dst, is_token_in_rank, dup_groups,
+// dup_loffs) are not touched and may be null; src_of_slot may be null when
+// the capacity E * (alignment - 1) is zero.
+int plan_empty(int E, int K, int R, int alignment, const MoePlanOut* out, cudaStream_t stream) {
+    if (check_sizes(0, E, K, R) != MOE_OK || alignment < 1 || out == nullptr) return MOE_ERR_INVALID_ARG;
+    const int64_t p_cap = moe_plan_capacity_rows(0, E, K, alignment);
+    if (p_cap < 0 || p_cap >= (int64_t(1) << 31) - 1) return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {out->tokens_per_expert, out->cu_seqlens,        out->zero_fill_ranges, out->pairs_per_rank,
+                          out->tokens_per_rank,   out->rank_prefix,       out->rank_slot_offsets, out->dup_counts,
+                          out->status};
+    for (const void* p : ptrs)
+        if (p == nullptr || !aligned(p, 4)) return MOE_ERR_INVALID_ARG;
+    if (p_cap > 0 && (out->src_of_slot == nullptr || !aligned(out->src_of_slot, 4))) return MOE_ERR_INVALID_ARG;
+    int64_t blocks = (p_cap + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(moe_host::num_sms()) * 4;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return moe_host::launch(moe::plan_empty_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, *out, E,
+                            R, p_cap);
+}
+
+}  // namespace
+
 extern "C" MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, int R, int alignment,
                                 void* workspace, size_t workspace_bytes, const MoePlanOut* out,
                                 cudaStream_t stream) {
+    if (N == 0) return plan_empty(E, K, R, alignment, out, stream);
     PlanArgs a;
     int rc = plan_args(topk_idx, N, E, K, R, alignment, workspace, workspace_bytes, out, &a);
     if (rc != MOE_OK) return rc;
@@ -2210,6 +2272,7 @@ extern "C" MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, in
 // ---------------------------------------------------------------- fused route + plan
 extern "C" MOE_API int moe_route_plan_fused(int N, int E, int K, int R, int n_group) {
     if (check_sizes(N, E, K, R) != MOE_OK) return -1;
+    if (N == 0) return 0;  // nothing to route: the plan alone runs
     if (ensure_kernel_attributes() != MOE_OK) return -1;
     // opt-in: on GB300 the fused launch measured slower than the two calls
     // (routing on the plan's 16 SMs costs what the routing kernel costs on

@@ -168,6 +168,7 @@ extern "C" MOE_API int moe_route_topk(const float* logits, const float* bias, in
     const int rc = moe_host::route_args(logits, bias, N, E, K, scoring, renormalize, n_group, topk_group,
                                         routed_scaling, topk_idx, topk_w, &a);
     if (rc != MOE_OK) return rc;
+    if (N == 0) return MOE_OK;  // an empty batch: nothing to route, no launch
     if (route_fast_applies(a))
         return a.scoring == MOE_SCORING_SOFTMAX ? dispatch_route_fast<true>(a, stream)
                                                 : dispatch_route_fast<false>(a, stream);

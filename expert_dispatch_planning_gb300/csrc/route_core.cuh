@@ -488,8 +488,9 @@ inline int route_args(const float* logits, const float* bias, int N, int E, int 
                       int n_group, int topk_group, float routed_scaling, int32_t* topk_idx, float* topk_w,
                       moe::RouteArgs* a) {
     auto aligned = [](const void* p, uintptr_t al) { return (reinterpret_cast<uintptr_t>(p) % al) == 0; };
-    if (logits == nullptr || topk_idx == nullptr || topk_w == nullptr) return MOE_ERR_INVALID_ARG;
-    if (N < 1 || E < 1 || E > 1024 || K < 1 || K > 32 || K > E) return MOE_ERR_INVALID_ARG;
+    // N = 0 (an empty batch) is valid; its zero-sized arrays may be null
+    if (N > 0 && (logits == nullptr || topk_idx == nullptr || topk_w == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (N < 0 || E < 1 || E > 1024 || K < 1 || K > 32 || K > E) return MOE_ERR_INVALID_ARG;
     if (scoring != MOE_SCORING_SOFTMAX && scoring != MOE_SCORING_SIGMOID) return MOE_ERR_INVALID_ARG;
     if (n_group < 1 || n_group > 32) return MOE_ERR_INVALID_ARG;
     if (static_cast<int64_t>(N) * K >= (int64_t(1) << 31) || static_cast<int64_t>(N) * E >= (int64_t(1) << 40))

@@ -312,17 +312,21 @@ constexpr size_t kSmemPerSm = 227 * 1024;
 
 extern "C" MOE_API int moe_permute(const uint16_t* x, int N, int H, int K, int E, int alignment,
                                    const MoePlanOut* plan, uint16_t* permuted, int flags, cudaStream_t stream) {
-    if (x == nullptr || plan == nullptr || permuted == nullptr || plan->dst == nullptr ||
-        plan->zero_fill_ranges == nullptr || plan->status == nullptr)
+    // N = 0 (an empty batch): no rows to move and, with every expert empty,
+    // no padding rows to zero; nothing is written, so x, dst and permuted
+    // (E * (alignment - 1) rows, none when alignment is 1) may be null
+    if (plan == nullptr || plan->zero_fill_ranges == nullptr || plan->status == nullptr ||
+        (N > 0 && (x == nullptr || permuted == nullptr || plan->dst == nullptr)))
         return MOE_ERR_INVALID_ARG;
     if ((flags & ~MOE_PERMUTE_EARLY_X) != 0) return MOE_ERR_INVALID_ARG;
-    if (N < 1 || K < 1 || K > 32 || E < 1 || E > 1024 || K > E || alignment < 1 || H < 8 || H % 8 != 0)
+    if (N < 0 || K < 1 || K > 32 || E < 1 || E > 1024 || K > E || alignment < 1 || H < 8 || H % 8 != 0)
         return MOE_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(permuted, 16) || !aligned(plan->dst, 4)) return MOE_ERR_INVALID_ARG;
     const int64_t p_cap = moe_plan_capacity_rows(N, E, K, alignment);
     if (p_cap < 0 || p_cap >= (int64_t(1) << 31) - 1) return MOE_ERR_INVALID_ARG;
     const int64_t row_bytes = static_cast<int64_t>(H) * 2;
     if (row_bytes > 96 * 1024) return MOE_ERR_UNSUPPORTED;
+    if (N == 0) return MOE_OK;
 
     moe::PermuteArgs a;
     a.x = x;
@@ -399,15 +403,17 @@ int launch_combine(const moe::CombineArgs& a, cudaStream_t stream) {
 
 extern "C" MOE_API int moe_combine(const uint16_t* y, const float* topk_w, int N, int K, int H, int E,
                                    int alignment, const MoePlanOut* plan, uint16_t* out, cudaStream_t stream) {
-    if (y == nullptr || topk_w == nullptr || plan == nullptr || out == nullptr || plan->dst == nullptr ||
-        plan->status == nullptr)
+    // N = 0 (an empty batch): no output rows; the N-sized arrays may be null
+    if (plan == nullptr || plan->status == nullptr ||
+        (N > 0 && (y == nullptr || topk_w == nullptr || out == nullptr || plan->dst == nullptr)))
         return MOE_ERR_INVALID_ARG;
-    if (N < 1 || K < 1 || K > 32 || E < 1 || E > 1024 || K > E || alignment < 1 || H < 8 || H % 8 != 0)
+    if (N < 0 || K < 1 || K > 32 || E < 1 || E > 1024 || K > E || alignment < 1 || H < 8 || H % 8 != 0)
         return MOE_ERR_INVALID_ARG;
     if (!aligned(y, 16) || !aligned(out, 16) || !aligned(topk_w, 4) || !aligned(plan->dst, 4))
         return MOE_ERR_INVALID_ARG;
     const int64_t p_cap = moe_plan_capacity_rows(N, E, K, alignment);
     if (p_cap < 0 || p_cap >= (int64_t(1) << 31) - 1) return MOE_ERR_INVALID_ARG;
+    if (N == 0) return MOE_OK;
     moe::CombineArgs a;
     a.y = y;
     a.w = topk_w;

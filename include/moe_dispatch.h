@@ -18,6 +18,9 @@
  *     that ran out) are recorded in the plan's device status word and read
  *     with moe_get_status().
  *   - Flat pair index f = s*K + k for token s and its k-th expert.
+ *   - N = 0 (a batch with no tokens) is valid everywhere N is taken, except
+ *     in the planning extensions (balanced plan, rank layout), which need
+ *     N >= 1.  Pointers to arrays that then have no elements may be NULL.
  *
  * Sources (page title and section):
  *   MoonEP moonep/planning.py -- PlanningKernel (histogram, per-expert
@@ -95,7 +98,8 @@ MOE_API const char* moe_status_string(int code);
  *                 ascending expert index.
  *   topk_w        (device) float32[N][K] out, within 1e-6 relative of the
  *                 exact value.
- * 1 <= N, 1 <= E <= 1024, E % 4 == 0 for the vector path (any E works).
+ * 0 <= N (N = 0 launches nothing), 1 <= E <= 1024, E % 4 == 0 for the
+ * vector path (any E works).
  * NaN logits are outside the contract (their position in the order is
  * unspecified).
  *
@@ -152,7 +156,8 @@ typedef struct MoePlanOut {
                                     cleared by moe_get_status.                            */
 } MoePlanOut;
 
-/* Rows the permuted buffer needs: N*K + E*(alignment-1).  -1 on bad input. */
+/* Rows the permuted buffer needs: N*K + E*(alignment-1) (N >= 0).  -1 on bad
+ * input. */
 MOE_API int64_t moe_plan_capacity_rows(int N, int E, int K, int alignment);
 
 /* Bytes of device workspace moe_plan needs for these sizes (0 on bad input). */
@@ -194,7 +199,11 @@ MOE_API int moe_plan_workspace_init(void* workspace, size_t workspace_bytes,
  *
  * Slots are canonical: within each expert, pairs keep ascending flat index
  * (MoonEP's stable scatter order), so the plan is a pure function of
- * topk_idx.  Checked here: N >= 1, 1 <= K <= 32, K <= E <= 1024,
+ * topk_idx.  N = 0 plans an empty batch in one small launch: every count,
+ * offset and prefix is 0, zero_fill_ranges are (0, 0), src_of_slot is -1 on
+ * all E*(alignment-1) rows; topk_idx, the workspace and the N-sized arrays
+ * are not touched (NULL allowed), nor src_of_slot when alignment is 1.
+ * Checked here: N >= 0, 1 <= K <= 32, K <= E <= 1024,
  * E % R == 0, R <= 128, N*K < 2^30, P_cap < 2^31.  Recorded in the status
  * word by the device: MOE_ERR_DEVICE_INDEX (an expert id outside [0, E)),
  * MOE_ERR_WORKSPACE (a workspace that was never initialised),

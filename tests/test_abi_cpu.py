@@ -57,7 +57,11 @@ def test_status_strings(lib):
 def test_sizes(lib):
     assert lib.moe_plan_capacity_rows(4, 4, 2, 2) == 12
     assert lib.moe_plan_capacity_rows(65536, 256, 8, 128) == 65536 * 8 + 256 * 127
-    assert lib.moe_plan_capacity_rows(0, 4, 2, 2) == -1
+    assert lib.moe_plan_capacity_rows(0, 4, 2, 2) == 4      # an empty batch: E*(a-1) rows
+    assert lib.moe_plan_capacity_rows(-1, 4, 2, 2) == -1
+    assert lib.moe_plan_workspace_size(0, 8, 2, 2) > 0
+    assert lib.moe_plan_launch_count(0, 8, 2, 2) == 1        # the empty-plan kernel
+    assert lib.moe_plan_launch_count(-1, 8, 2, 2) == -1
     ws = lib.moe_plan_workspace_size(4096, 256, 8, 8)
     assert ws > 0 and ws % 16 == 0
     assert lib.moe_plan_workspace_size(4096, 256, 8, 7) == 0      # E % R
@@ -79,7 +83,12 @@ def test_route_rejects_bad_arguments(lib):
         return f(a["logits"], a["bias"], a["N"], a["E"], a["K"], a["scoring"], a["renorm"], a["ng"],
                  a["tg"], a["sc"], a["idx"], a["w"], a["stream"])
     assert call(logits=None) == 1
-    assert call(N=0) == 1
+    assert call(N=-1) == 1
+    assert call(N=0, E=2048) == 1                     # an empty batch is still validated
+    # an empty batch is valid, launches nothing (so it runs without a GPU),
+    # and its zero-sized arrays may be NULL
+    assert call(N=0) == 0
+    assert call(N=0, logits=None, idx=None, w=None) == 0
     assert call(K=9) == 1
     assert call(K=33, E=64) == 1
     assert call(E=2048) == 1
@@ -112,6 +121,17 @@ def test_plan_rejects_bad_arguments(lib):
     bad = _plan_struct()
     bad.dst = None
     assert call(o=ctypes.byref(bad)) == 1
+    assert call(N=-1) == 1
+    # an empty batch: still validated (its kernel needs a GPU, so only the
+    # rejections run here)
+    assert call(N=0, o=None) == 1
+    assert call(N=0, R=3) == 1
+    no_cu = _plan_struct()
+    no_cu.cu_seqlens = None
+    assert call(N=0, o=ctypes.byref(no_cu)) == 1
+    no_slots = _plan_struct()
+    no_slots.src_of_slot = None                        # capacity E*(a-1) = 8 rows
+    assert call(N=0, o=ctypes.byref(no_slots)) == 1
 
 
 def test_rows_reject_bad_arguments(lib):
@@ -123,6 +143,17 @@ def test_rows_reject_bad_arguments(lib):
     assert lib.moe_combine(FAKE, FAKE, 4, 2, 12, 8, 2, ctypes.byref(out), FAKE, None) == 1
     assert lib.moe_combine(FAKE, FAKE, 4, 9, 16, 8, 2, ctypes.byref(out), FAKE, None) == 1  # K > E
     assert lib.moe_combine(FAKE, FAKE, 4, 2, 16, 8, 2, None, FAKE, None) == 1
+    assert lib.moe_permute(FAKE, -1, 16, 2, 8, 2, ctypes.byref(out), FAKE, 0, None) == 1
+    assert lib.moe_combine(FAKE, FAKE, -1, 2, 16, 8, 2, ctypes.byref(out), FAKE, None) == 1
+    # an empty batch moves no rows: valid, nothing launched, N-sized arrays may be NULL
+    empty = _plan_struct()
+    empty.dst = None
+    assert lib.moe_permute(None, 0, 16, 2, 8, 2, ctypes.byref(empty), FAKE, 0, None) == 0
+    assert lib.moe_permute(None, 0, 16, 2, 8, 1, ctypes.byref(empty), None, 0, None) == 0   # no capacity rows
+    assert lib.moe_permute(None, 4, 16, 2, 8, 2, ctypes.byref(out), FAKE, 0, None) == 1     # x needed
+    assert lib.moe_permute(None, 0, 12, 2, 8, 2, ctypes.byref(empty), FAKE, 0, None) == 1    # H % 8
+    assert lib.moe_combine(FAKE, None, 0, 2, 16, 8, 2, ctypes.byref(empty), None, None) == 0
+    assert lib.moe_combine(FAKE, None, 0, 9, 16, 8, 2, ctypes.byref(empty), None, None) == 1  # K > E
 
 
 def test_debug_hook_validates(lib):

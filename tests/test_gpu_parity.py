@@ -400,6 +400,38 @@ def test_end_to_end(m, name):
     assert np.mean(g != o) < 1e-3
 
 
+@pytest.mark.parametrize("E,K,R,a", [(8, 2, 2, 8), (256, 8, 64, 128), (4, 1, 1, 1), (6, 3, 3, 5)])
+def test_empty_batch(m, E, K, R, a):
+    """A batch with no tokens: routing launches nothing, the plan equals the
+    oracle's empty plan (every output written over a sentinel), permute and
+    combine move no rows and leave the permuted buffer as it was, and the
+    plan's tile map and copy work."""
+    p = m.Plan.allocate(0, E, K, R, a)
+    for k in PLAN_KEYS:
+        t = getattr(p, k)
+        if t.dtype == torch.int32:
+            t.fill_(0x5A5A5A5A)
+    logits = torch.empty((0, E), dtype=torch.float32, device=dev())
+    idx, wts, p = m.route_plan(logits, K, R, a, out=p)
+    assert idx.shape == (0, K) and wts.shape == (0, K)
+    assert m.route_plan_launches(0, E, K, R) == 1 == m.plan_launches(0, E, K, R)
+    want = oracle.plan(np.zeros((0, K), np.int32), E, R, a)
+    assert_plan_equal(p.to_host(), want)
+
+    H = 64
+    x = torch.empty((0, H), dtype=torch.bfloat16, device=dev())
+    perm = torch.full((p.P_cap, H), 1.5, dtype=torch.bfloat16, device=dev())
+    m.permute(x, p, out=perm, early_x=True)
+    out = m.combine(perm, wts, p)
+    assert out.shape == (0, H)
+    assert bool((perm == 1.5).all())
+    te, tl, sizes = m.tile_map(p)
+    assert sizes.tolist() == [0, 0] and bool((te == -1).all()) and bool((tl == -1).all())
+    c = p.clone()
+    assert_plan_equal(c.to_host(), want)
+    assert m.get_status(p) == 0 and m.get_status(c) == 0
+
+
 def test_plan_reuse_and_copy(m):
     """A plan serves several permute/combine calls; a copied plan is identical
     and keeps working after the original's buffers are overwritten."""

@@ -94,3 +94,21 @@ def test_plan_argument_errors():
         oracle.plan(topk + 9, 8, 2, 1)       # id out of range
     with pytest.raises(oracle.OracleError):
         oracle.plan(topk, 8, 2, 0)           # alignment
+
+
+@pytest.mark.parametrize("E,K,R,a", [(8, 2, 2, 8), (256, 8, 64, 128), (4, 1, 1, 1), (6, 3, 3, 5)])
+def test_empty_batch(E, K, R, a):
+    # no tokens: every count, offset and prefix is zero, no expert is padded
+    # (an expert with no pairs pads to zero rows), and all E*(a-1) rows of
+    # the capacity are unused; the counting definition agrees
+    topk = np.zeros((0, K), np.int32)
+    p = oracle.plan(topk, E, R, a)
+    assert p["P"] == 0 and p["P_cap"] == E * (a - 1)
+    for k in ("tokens_per_expert", "cu_seqlens", "zero_fill_ranges", "pairs_per_rank", "tokens_per_rank",
+              "rank_prefix", "rank_slot_offsets", "dup_counts"):
+        assert not np.asarray(p[k]).any(), k
+    assert p["cu_seqlens"].shape == (E + 1,) and p["rank_prefix"].shape == (R + 1,)
+    assert p["src_of_slot"].tolist() == [-1] * (E * (a - 1))
+    assert p["dst"].shape == (0, K) and p["is_token_in_rank"].shape == (0, R)
+    assert len(p["dup_groups"]) == 0 and len(p["dup_loffs"]) == 0
+    _same(p, definition_plan(topk, E, R, a))
