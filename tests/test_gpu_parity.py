@@ -345,7 +345,8 @@ def test_permute_combine_large_sampled(m):
 
 @pytest.mark.parametrize("N,E,K,R,H,a", [(1, 8, 2, 2, 8, 4), (37, 8, 3, 4, 24, 1), (500, 16, 5, 4, 136, 8),
                                           (1000, 64, 7, 8, 72, 16), (300, 32, 16, 8, 512, 3),
-                                          (129, 64, 32, 4, 64, 2), (2000, 8, 1, 8, 1024, 64)])
+                                          (129, 64, 32, 4, 64, 2), (2000, 8, 1, 8, 1024, 64),
+                                          (40, 8, 3, 2, 49152, 4)])   # the largest row: 96 KB
 def test_permute_combine_shapes(m, N, E, K, R, H, a):
     rng = np.random.default_rng(N * 7 + K)
     topk = workloads.random_topk(rng, N, E, K)
