@@ -22,18 +22,23 @@ bool pdl_enabled() {
     return on;
 }
 
+// SM count of the current device, cached per device (safe for concurrent
+// callers); GB300's 152 if the query fails.
 int num_sms() {
+    constexpr int kFallback = 152;
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int> cache[kMaxDevices];  // 0: not queried yet
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-    static int cached_dev = -1;
-    static int cached = 0;
-    if (dev != cached_dev) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-        cached = n;
-        cached_dev = dev;
+    if (cudaGetDevice(&dev) != cudaSuccess) return kFallback;
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    if (cached) {
+        const int n = cache[dev].load(std::memory_order_relaxed);
+        if (n > 0) return n;
     }
-    return cached;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = kFallback;
+    if (cached) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
 }
 
 int64_t timeout_ns() { return g_timeout_ns.load(); }

@@ -6,6 +6,7 @@
 // route_fast_kernel (route_fast.cuh): E = 32 G, sigmoid over groups of 32
 // experts or renormalised softmax, selection by approximate keys proved
 // exact, the exact router as the per-token fallback; bit-identical output.
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 
@@ -131,14 +132,14 @@ int launch_route_fast(const RouteArgs& a, cudaStream_t stream) {
     const int64_t batches = (static_cast<int64_t>(a.N) + tokens_per_block - 1) / tokens_per_block;
     const size_t smem = sizeof(float) * (32 * G + moe::RF_WARPS * 1024);
     // one wave of resident blocks, the same number of batches for every block
-    static int per_sm = 0;
+    static std::atomic<int> per_sm_cache{0};  // the same for every GB300; 0: not queried yet
+    int per_sm = per_sm_cache.load(std::memory_order_relaxed);
     if (per_sm == 0) {
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, moe::route_fast_kernel<G, SM>, moe::RF_THREADS, smem) !=
-                cudaSuccess ||
-            n < 1)
-            n = 1;
-        per_sm = n;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe::route_fast_kernel<G, SM>, moe::RF_THREADS,
+                                                          smem) != cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        per_sm_cache.store(per_sm, std::memory_order_relaxed);
     }
     const int64_t cap = static_cast<int64_t>(moe_host::num_sms()) * per_sm;
     const int64_t rounds = (batches + cap - 1) / cap;
