@@ -337,17 +337,21 @@ bool aligned4(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_
 extern "C" MOE_API int moe_plan_balanced(const MoePlanOut* plan, const int32_t* topk_idx, int N, int E, int K,
                                          int R, int token_padding, int32_t capacity, int B, int32_t NvS,
                                          const MoeBalancedPlanOut* out, cudaStream_t stream) {
-    if (plan == nullptr || out == nullptr || topk_idx == nullptr) return MOE_ERR_INVALID_ARG;
-    if (N < 1 || E < 1 || E > 1024 || K < 1 || K > 32 || K > E || R < 1 || R > 128 || E % R != 0)
+    // N = 0 (an empty batch) is valid: no pairs to balance, every output
+    // matrix zero and no redundant expert; topk_idx and the dst arrays have
+    // no elements and may be null
+    if (plan == nullptr || out == nullptr || (N > 0 && topk_idx == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (N < 0 || E < 1 || E > 1024 || K < 1 || K > 32 || K > E || R < 1 || R > 128 || E % R != 0)
         return MOE_ERR_INVALID_ARG;
     if (static_cast<int64_t>(N) * K >= (int64_t(1) << 30)) return MOE_ERR_INVALID_ARG;
     if (token_padding < 1 || B < 0 || B > moe::BAL_MAX_B || NvS < 1 || capacity < 0) return MOE_ERR_INVALID_ARG;
     if (static_cast<int64_t>(R) * NvS >= (int64_t(1) << 31)) return MOE_ERR_INVALID_ARG;
-    const void* in[] = {plan->tokens_per_expert, plan->cu_seqlens, plan->dst, plan->status, topk_idx};
+    const void* in[] = {plan->tokens_per_expert, plan->cu_seqlens, plan->status};
     for (const void* p : in)
         if (!aligned4(p)) return MOE_ERR_INVALID_ARG;
+    if (N > 0 && (!aligned4(plan->dst) || !aligned4(topk_idx) || !aligned4(out->dst))) return MOE_ERR_INVALID_ARG;
     const void* outs[] = {out->z, out->alloc, out->alloc_cumsum, out->remote_stats, out->rank_cu_seqlens,
-                          out->rank_zero_fill, out->expert_offsets, out->dst};
+                          out->rank_zero_fill, out->expert_offsets};
     for (const void* p : outs)
         if (!aligned4(p)) return MOE_ERR_INVALID_ARG;
     if (B > 0 && !aligned4(out->experts_to_copy)) return MOE_ERR_INVALID_ARG;
@@ -381,6 +385,7 @@ extern "C" MOE_API int moe_plan_balanced(const MoePlanOut* plan, const int32_t* 
     rc = moe_host::launch(moe::balance_groups_kernel, dim3((R + moe::BAL_GRP_WARPS - 1) / moe::BAL_GRP_WARPS),
                           dim3(moe::BAL_GRP_WARPS * 32), 0, stream, a);
     if (rc != MOE_OK) return rc;
+    if (N == 0) return MOE_OK;  // no pairs: no dst to write
     const int64_t warps = (static_cast<int64_t>(N) + 32 / K - 1) / (32 / K);
     const unsigned blocks = static_cast<unsigned>((warps * 32 + moe::BAL_DST_THREADS - 1) / moe::BAL_DST_THREADS);
     return moe_host::launch(moe::balance_dst_kernel, dim3(blocks), dim3(moe::BAL_DST_THREADS), 0, stream, a);

@@ -236,6 +236,17 @@ __global__ void __launch_bounds__(LAYOUT_THREADS) rank_layout_slot_kernel(const 
     }
 }
 
+// An empty batch (N = 0): every channel prefix is zero.  Writes nothing
+// after a failed plan, like the other layout kernels.
+__global__ void __launch_bounds__(LAYOUT_THREADS) rank_layout_empty_kernel(int32_t* cpm, const int32_t* status,
+                                                                         int64_t n) {
+    pdl_wait();
+    pdl_trigger();
+    if (ld_volatile_s32(status) != 0) return;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) cpm[i] = 0;
+}
+
 }  // namespace moe
 
 extern "C" MOE_API int moe_tile_map(const MoePlanOut* plan, int E, int alignment, int32_t* tile_expert,
@@ -289,6 +300,7 @@ size_t layout_ws_bytes(int N, int R) {
 }  // namespace
 
 extern "C" MOE_API size_t moe_rank_layout_workspace_size(int N, int R) {
+    if (N == 0 && R >= 1 && R <= 128) return 256;  // an empty batch reads no workspace
     if (N < 1 || R < 1 || R > 128 || static_cast<int64_t>(N) * R >= (int64_t(1) << 31)) return 0;
     return layout_ws_bytes(N, R);
 }
@@ -296,8 +308,19 @@ extern "C" MOE_API size_t moe_rank_layout_workspace_size(int N, int R) {
 extern "C" MOE_API int moe_rank_layout(const MoePlanOut* plan, int N, int R, int num_channels, void* workspace,
                                        size_t workspace_bytes, int32_t* channel_prefix_matrix,
                                        int32_t* token_rank_slot, cudaStream_t stream) {
-    if (plan == nullptr || plan->is_token_in_rank == nullptr || plan->rank_prefix == nullptr ||
-        plan->status == nullptr || channel_prefix_matrix == nullptr || token_rank_slot == nullptr ||
+    if (plan == nullptr || plan->status == nullptr || channel_prefix_matrix == nullptr) return MOE_ERR_INVALID_ARG;
+    if (N == 0) {
+        // an empty batch: no channel holds a token; is_token_in_rank,
+        // token_rank_slot and the workspace are not touched (NULL allowed)
+        if (R < 1 || R > 128 || num_channels < 1) return MOE_ERR_INVALID_ARG;
+        const int64_t n = static_cast<int64_t>(R) * num_channels;
+        int64_t blocks = (n + moe::LAYOUT_THREADS - 1) / moe::LAYOUT_THREADS;
+        const int64_t cap = static_cast<int64_t>(moe_host::num_sms()) * 4;
+        if (blocks > cap) blocks = cap;
+        return moe_host::launch(moe::rank_layout_empty_kernel, dim3(static_cast<unsigned>(blocks)),
+                                dim3(moe::LAYOUT_THREADS), 0, stream, channel_prefix_matrix, plan->status, n);
+    }
+    if (plan->is_token_in_rank == nullptr || plan->rank_prefix == nullptr || token_rank_slot == nullptr ||
         workspace == nullptr)
         return MOE_ERR_INVALID_ARG;
     if (N < 1 || R < 1 || R > 128 || num_channels < 1 || static_cast<int64_t>(N) * R >= (int64_t(1) << 31))

@@ -18,9 +18,8 @@
  *     that ran out) are recorded in the plan's device status word and read
  *     with moe_get_status().
  *   - Flat pair index f = s*K + k for token s and its k-th expert.
- *   - N = 0 (a batch with no tokens) is valid everywhere N is taken, except
- *     in the planning extensions (balanced plan, rank layout), which need
- *     N >= 1.  Pointers to arrays that then have no elements may be NULL.
+ *   - N = 0 (a batch with no tokens) is valid everywhere N is taken.
+ *     Pointers to arrays that then have no elements may be NULL.
  *
  * Sources (page title and section):
  *   MoonEP moonep/planning.py -- PlanningKernel (histogram, per-expert
@@ -284,7 +283,9 @@ typedef struct MoeBalancedPlanOut {
  * token_padding  rows each group is padded to (>= 1).
  * NvS          rows per rank in the dst encoding; R*NvS < 2^31.  A rank whose
  *              groups need more rows sets MOE_ERR_DEVICE_CAPACITY.
- * Two launches on `stream` after the plain plan; no workspace.
+ * Three launches on `stream` after the plain plan (two when N = 0: nothing
+ * to balance, every matrix zero, every experts_to_copy entry -1; topk_idx
+ * and the dst arrays may then be NULL); no workspace.
  */
 MOE_API int moe_plan_balanced(const MoePlanOut* plan, const int32_t* topk_idx, int N, int E, int K, int R,
                               int token_padding, int32_t capacity, int B, int32_t NvS,
@@ -320,7 +321,9 @@ MOE_API int moe_tile_map(const MoePlanOut* plan, int E, int alignment, int32_t* 
  *                   (every call rewrites what it reads).  Calls sharing a
  *                   workspace must not overlap on the GPU.
  * Reads the plan's is_token_in_rank and rank_prefix.  R <= 128.  Two kernel
- * launches.  MOE_ERR_CAPACITY if the workspace is too small.
+ * launches.  MOE_ERR_CAPACITY if the workspace is too small.  N = 0: one
+ * launch that zeroes channel_prefix_matrix; is_token_in_rank,
+ * token_rank_slot and the workspace are not touched (NULL allowed).
  */
 MOE_API size_t moe_rank_layout_workspace_size(int N, int R);
 MOE_API int moe_rank_layout(const MoePlanOut* plan, int N, int R, int num_channels, void* workspace,

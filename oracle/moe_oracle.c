@@ -584,7 +584,7 @@ int orc_plan_balanced(const int32_t* topk, int N, int E, int K, int R, int token
                       int32_t* rank_cu_seqlens /* R*(E+B) */, int32_t* rank_zero_fill /* R*(E+B)*2 */,
                       int32_t* expert_offsets /* R*E */, int32_t* dst /* N*K */)
 {
-    if (N < 1 || E < 1 || K < 1 || R < 1 || E % R != 0 || token_padding < 1 || B < 0 || NvS < 1)
+    if (N < 0 || E < 1 || K < 1 || R < 1 || E % R != 0 || token_padding < 1 || B < 0 || NvS < 1)
         return ORC_EINVAL;
     const int epn = E / R;
     const int64_t NK = (int64_t)N * K;
@@ -817,7 +817,7 @@ int orc_tile_map(const int32_t* counts, int E, int tile, int32_t* tile_expert, i
 int orc_rank_layout(const uint8_t* is_token_in_rank, int N, int R, int C, int32_t* channel_prefix_matrix,
                     int32_t* token_rank_slot)
 {
-    if (N < 1 || R < 1 || C < 1)
+    if (N < 0 || R < 1 || C < 1)
         return ORC_EINVAL;
     int64_t q = ((int64_t)N + C - 1) / C;
     int32_t base = 0;

@@ -165,7 +165,9 @@ def test_rank_layout_workspace_and_validation(lib):
     n = lib.moe_rank_layout_workspace_size(65536, 64)
     assert n > 0 and n % 4 == 0
     assert lib.moe_rank_layout_workspace_size(1, 1) > 0
-    assert lib.moe_rank_layout_workspace_size(0, 4) == 0
+    assert lib.moe_rank_layout_workspace_size(0, 4) > 0        # an empty batch
+    assert lib.moe_rank_layout_workspace_size(-1, 4) == 0
+    assert lib.moe_rank_layout_workspace_size(0, 129) == 0
     assert lib.moe_rank_layout_workspace_size(16, 129) == 0
     out = _plan_struct()
     f = lib.moe_rank_layout
@@ -178,3 +180,7 @@ def test_rank_layout_workspace_and_validation(lib):
     assert call(ws=P(0x10010)) == 1                   # 256-byte alignment
     assert call(ws_bytes=4) == 3                      # too small
     assert call(trs=None) == 1
+    assert call(N=-1) == 1
+    assert call(N=0, C=0) == 1                        # an empty batch is still validated
+    assert call(N=0, R=129) == 1
+    assert call(N=0, cpm=None) == 1

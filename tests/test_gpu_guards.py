@@ -104,7 +104,7 @@ def check_plan(arr, want, K):
 # the default path of each size class, and the paths MOE_PLAN_PATH can force
 @pytest.mark.parametrize("path", ["auto", "small", "medium", "cluster", "grid", "lookback"])
 @pytest.mark.parametrize("N,E,K,R,a", [(5000, 8, 2, 4, 16), (3000, 128, 8, 8, 128), (20000, 256, 8, 64, 128),
-                                       (777, 6, 3, 3, 5), (1, 1024, 32, 128, 2)])
+                                       (777, 6, 3, 3, 5), (1, 1024, 32, 128, 2), (0, 256, 8, 64, 128)])
 def test_plan_writes_only_its_arrays(lib, monkeypatch, path, N, E, K, R, a):
     monkeypatch.setenv("MOE_PLAN_PATH", path)
     rng = np.random.default_rng(N + E)

@@ -406,7 +406,8 @@ def test_empty_batch(m, E, K, R, a):
     """A batch with no tokens: routing launches nothing, the plan equals the
     oracle's empty plan (every output written over a sentinel), permute and
     combine move no rows and leave the permuted buffer as it was, and the
-    plan's tile map and copy work."""
+    plan's tile map, copy, rank layout and balanced plan equal the oracle's
+    (all empty or zero)."""
     p = m.Plan.allocate(0, E, K, R, a)
     for k in PLAN_KEYS:
         t = getattr(p, k)
@@ -430,6 +431,13 @@ def test_empty_batch(m, E, K, R, a):
     assert sizes.tolist() == [0, 0] and bool((te == -1).all()) and bool((tl == -1).all())
     c = p.clone()
     assert_plan_equal(c.to_host(), want)
+    cpm, trs = m.rank_layout(p, 5)
+    assert cpm.shape == (R, 5) and not bool(cpm.any()) and trs.shape == (0, R)
+    B = 2
+    b = m.plan_balanced(idx, p, a, 0, B, 64).to_host()
+    o_b = oracle.plan_balanced(np.zeros((0, K), np.int32), E, R, a, 0, B, 64)
+    for k, v in o_b.items():
+        assert np.array_equal(b[k].reshape(v.shape), v), k
     assert m.get_status(p) == 0 and m.get_status(c) == 0
 
 
@@ -450,3 +458,41 @@ def test_plan_reuse_and_copy(m):
         out = m.combine(perm, w32, c)
         assert np.array_equal(bits(out), oracle.combine(o_perm, o_w.astype(np.float32), want["dst"]))
     assert m.get_status(c) == 0
+
+
+def test_concurrent_callers_on_separate_streams(m):
+    """Host threads calling the library at once (ctypes releases the GIL), each
+    on its own stream with its own plan buffers and workspace: every result
+    equals the oracle's.  Covers the library's host-side caches (SM count,
+    kernel attributes, path choice) under concurrent first use."""
+    import threading
+    shapes = [(3000, 8, 2, 4, 16), (2000, 128, 8, 8, 128), (20000, 256, 8, 64, 128), (777, 6, 3, 3, 5)]
+    errors = []
+
+    def worker(tid):
+        try:
+            rng = np.random.default_rng(1000 + tid)
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                for it in range(6):
+                    N, E, K, R, a = shapes[(tid + it) % len(shapes)]
+                    topk = workloads.random_topk(rng, N, E, K, hot=0.5)
+                    p = m.plan(torch.from_numpy(topk).to(dev()), E, R, a)
+                    H = 64
+                    x_bits = workloads.make_x_bits(rng, N, H)
+                    perm = m.permute(to_bf16(x_bits), p)
+                    got = p.to_host()
+                    want = oracle.plan(topk, E, R, a)
+                    assert_plan_equal(got, want)
+                    o_perm = oracle.permute(x_bits, want["dst"], want["zero_fill_ranges"], K, want["P_cap"])
+                    assert np.array_equal(bits(perm)[: want["P"]], o_perm[: want["P"]])
+                    assert m.get_status(p, stream=stream) == 0
+        except Exception as e:  # reported on the main thread
+            errors.append((tid, repr(e)))
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors

@@ -63,3 +63,15 @@ def test_capacity_too_small_is_an_error():
     topk = np.zeros((64, 1), np.int32)
     with pytest.raises(oracle.OracleError):
         oracle.plan_balanced(topk, 4, 2, 1, 100, 1, NvS=32)
+
+
+@pytest.mark.parametrize("E,K,R,tp,cap,B", [(8, 2, 4, 16, 0, 2), (64, 6, 8, 1, 5, 0), (256, 8, 64, 128, 100, 4)])
+def test_empty_batch(E, K, R, tp, cap, B):
+    # no tokens: nothing to move (z = 0), no rank handles a pair (alloc and
+    # its prefix 0), no remote expert has pairs so no redundant expert is
+    # chosen (-1), and every group is empty (offsets, ends, padding 0)
+    o = oracle.plan_balanced(np.zeros((0, K), np.int32), E, R, tp, cap, B, 64)
+    for k in ("z", "alloc", "alloc_cumsum", "remote_stats", "rank_cu_seqlens", "rank_zero_fill", "expert_offsets"):
+        assert not o[k].any(), k
+    assert o["experts_to_copy"].shape == (R, B) and (o["experts_to_copy"] == -1).all()
+    assert o["rank_cu_seqlens"].shape == (R, E + B) and o["dst"].shape == (0, K)

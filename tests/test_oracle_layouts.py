@@ -57,3 +57,10 @@ def test_rank_layout_invariants(seed):
         rows = np.nonzero(itr[:, r])[0]
         assert trs[rows, r].tolist() == list(range(prefix[r], prefix[r + 1]))
         assert np.all(trs[itr[:, r] == 0, r] == -1)
+
+
+def test_rank_layout_empty_batch():
+    # no tokens: every channel is empty, so every prefix is zero
+    cpm, trs = oracle.rank_layout(np.zeros((0, 4), np.uint8), 3)
+    assert cpm.shape == (4, 3) and not cpm.any()
+    assert trs.shape == (0, 4)
