@@ -1,4 +1,4 @@
-"""Plans and rows at the largest sizes the host accepts.
+"""Routing, plans and rows at the largest sizes the host accepts.
 
 The oracle cannot plan at these sizes, so the plan checks are properties
 that determine the plan at any size, evaluated with torch on the device in
@@ -7,8 +7,9 @@ pairs and non-padding slots, ascending flat index within every expert (the
 canonical order), the duplicate rule per (token, rank), the rank matrices
 and the dedup totals.  The rows: every slot holds its token's row, every
 padding row is zero, rows from P on are untouched, and sampled tokens of the
-combine equal the oracle's combine of their gathered rows.  Inputs are
-seeded random ids drawn on the device.  Peak device memory: about 40 GB.
+combine equal the oracle's combine of their gathered rows.  Routing is per
+token, so sampled rows are compared with the oracle directly.  Inputs are
+seeded random values drawn on the device.  Peak device memory: about 55 GB.
 """
 import numpy as np
 import pytest
@@ -56,7 +57,6 @@ def check_plan_properties(p, topk, E, R, a):
     zf_start = torch.where(padded > counts, cu[:-1].to(torch.int32) + counts, torch.zeros_like(counts))
     assert torch.equal(p.zero_fill_ranges[:, 0], zf_start)
     assert torch.equal(p.zero_fill_ranges[:, 1], padded - counts)
-    cu32 = cu.to(torch.int32)
 
     dst = p.dst.reshape(-1)
     src = p.src_of_slot
@@ -76,7 +76,6 @@ def check_plan_properties(p, topk, E, R, a):
         e_slot = flat[s.clamp(min=0).to(torch.int64)]
         same = real[:-1] & real[1:] & (e_slot[:-1] == e_slot[1:])
         assert bool((s[1:][same] > s[:-1][same]).all())
-    del cu32
 
     # duplicates (an earlier k of the same token on the same rank), rank
     # matrices and (token, rank) group sizes, over chunks of tokens
@@ -160,3 +159,29 @@ def test_rows_with_a_permuted_buffer_above_2_30_rows(m):
     d_small = np.arange(256 * K, dtype=np.int32).reshape(256, K)
     want = oracle.combine(y_small, w[t].cpu().numpy(), d_small)
     assert np.array_equal(out.view(torch.int16)[t].cpu().numpy().view(np.uint16), want)
+
+
+@pytest.mark.parametrize("N,E,K,scoring,ng,tg,path", [
+    ((1 << 30) - 7, 8, 2, 0, 1, 1, "auto"),       # N*K just under 2^31; logits 34 GB
+    ((1 << 24) + 5, 256, 8, 1, 8, 4, "auto"),     # N*E above 2^32 elements; the approximate-key kernel
+    ((1 << 24) + 5, 256, 8, 1, 8, 4, "exact")])
+def test_route_at_the_limits(m, monkeypatch, N, E, K, scoring, ng, tg, path):
+    """Routing is per token, so sampled rows (and the last ones) are compared
+    with the oracle exactly: indices bit for bit, weights within 1e-6."""
+    monkeypatch.setenv("MOE_ROUTE_PATH", path)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(N % 1000)
+    logits = torch.randn((N, E), generator=g, device="cuda")
+    bias = None
+    if scoring == 1:
+        bias = torch.from_numpy(np.random.default_rng(7).uniform(-0.1, 0.1, E).astype(np.float32)).cuda()
+    idx, w = m.route_topk(logits, K, scoring=scoring, renormalize=True, bias=bias, n_group=ng, topk_group=tg,
+                          routed_scaling=2.5)
+    rows = np.concatenate([np.random.default_rng(8).choice(N, 4096, replace=False), np.arange(N - 64, N)])
+    t = torch.from_numpy(rows).cuda()
+    o_idx, o_w = oracle.route_topk(logits[t].cpu().numpy(), K, scoring=scoring, renormalize=True,
+                                   bias=None if bias is None else bias.cpu().numpy(), n_group=ng, topk_group=tg,
+                                   routed_scaling=2.5)
+    assert np.array_equal(idx[t].cpu().numpy(), o_idx)
+    err = np.abs(w[t].cpu().numpy().astype(np.float64) - o_w)
+    assert (err <= 1e-6 * np.abs(o_w) + 2.0 ** -126).all()
