@@ -167,7 +167,8 @@ MOE_API size_t moe_plan_workspace_size(int N, int E, int K, int R);
  * when R <= 32, E <= 256 and the plan fits one thread-block cluster of up to
  * 16 tiles (one tile = 32 warps x 1, 2, 4 or 8 steps x floor(32/K) tokens;
  * at most 4 steps when E > 32) that the GPU can co-schedule, else 2
- * (decoupled look-back, then the scatter).  -1 on bad sizes.  The
+ * (decoupled look-back, then the scatter); 1 for N = 0 (the empty plan).
+ * -1 on bad sizes.  The
  * environment variable MOE_PLAN_PATH=small|medium|cluster|grid|lookback
  * forces a path where the sizes allow it (cluster: a one-launch cluster
  * plan for any E; grid: one launch of up to 152 co-resident tiles); every
