@@ -184,3 +184,32 @@ def test_rank_layout_workspace_and_validation(lib):
     assert call(N=0, C=0) == 1                        # an empty batch is still validated
     assert call(N=0, R=129) == 1
     assert call(N=0, cpm=None) == 1
+
+
+def _header_prototypes():
+    """name -> list of parameter declarations, parsed from the header."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    protos = {}
+    for m in re.finditer(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(([^)]*)\)\s*;", text, flags=re.S):
+        params = [p.strip() for p in m.group(2).split(",") if p.strip()]
+        if params == ["void"]:
+            params = []
+        protos[m.group(1)] = params
+    return protos
+
+
+def test_binding_signatures_match_the_header():
+    # every ctypes declaration has the header's argument count, and pointer
+    # parameters are passed as pointers (a drift here would shift arguments)
+    import ctypes
+    from expert_dispatch_planning_gb300 import _lib
+    protos = _header_prototypes()
+    assert sorted(protos) == sorted(n for n, _, _ in _lib.SIGNATURES)
+    for name, _, argtypes in _lib.SIGNATURES:
+        params = protos[name]
+        assert len(argtypes) == len(params), (name, len(argtypes), params)
+        for decl, t in zip(params, argtypes):
+            is_ptr = "*" in decl or decl.startswith("cudaStream_t")
+            t_is_ptr = t in (ctypes.c_void_p, ctypes.c_char_p) or hasattr(t, "_type_") and t.__name__.startswith("LP_")
+            assert is_ptr == t_is_ptr, (name, decl, t)
