@@ -213,3 +213,27 @@ def test_binding_signatures_match_the_header():
             is_ptr = "*" in decl or decl.startswith("cudaStream_t")
             t_is_ptr = t in (ctypes.c_void_p, ctypes.c_char_p) or hasattr(t, "_type_") and t.__name__.startswith("LP_")
             assert is_ptr == t_is_ptr, (name, decl, t)
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    # a C99 caller: every declared entry point referenced, compiled by a C
+    # compiler and linked against the library (nothing is run)
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    cuda_inc = "/usr/local/cuda/include"
+    names = declared_functions()
+    src = tmp_path / "caller.c"
+    src.write_text('#include "moe_dispatch.h"\n#include <stdio.h>\n'
+                   "int main(void) {\n    const void* fns[] = {\n" +
+                   "".join("        (const void*)&%s,\n" % n for n in names) +
+                   "    };\n    printf(\"%%s\\n\", moe_status_string(MOE_OK));\n"
+                   "    return (int)(sizeof(fns) / sizeof(fns[0])) == %d ? 0 : 1;\n}\n" % len(names))
+    libdir = os.path.dirname(lib._name)
+    cmd = [gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+           "-I", cuda_inc, str(src), "-o", str(tmp_path / "caller"), "-L", libdir, "-lmoe_dispatch",
+           "-Wl,-rpath," + libdir]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
