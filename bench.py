@@ -5,12 +5,17 @@ One step = route_topk + plan (2 launches) + permute + combine over one batch
 of a synthetic workload already resident in HBM (experts are the identity:
 the combine reads the permuted buffer back).  Prints one JSON line.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config mixtral]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config large]
   python bench.py --impl reference ...   # the CPU oracle on the host cores
 
-Multi-GPU runs (torchrun, one rank per GPU) are independent replicas of the
-same workload on every rank (the path has no exchange step on one node's
-logical ranks): value = all ranks' tokens / the slowest rank's time.
+The default workload is the large dedup-heavy one (N=65536, E=256, K=8,
+R=64, H=7168); --config picks one of the other four.
+
+Multi-GPU runs are independent replicas of the same workload on every rank
+(the path has no exchange step on one node's logical ranks): value = all
+ranks' tokens / the slowest rank's time.  Under torchrun the ranks come from
+the environment; a plain ``python bench.py --gpus N`` (N > 1) starts the N
+ranks itself through torch.distributed.run on 127.0.0.1.
 """
 from __future__ import annotations
 
@@ -226,6 +231,17 @@ def cpu_baseline(w, inp, min_seconds=10.0, max_steps=40):
 
 def run_reference(args, w):
     ws, rank, _ = dist_env()
+    n_ranks = ws
+    if ws > 1:
+        # the ranks meet once (gloo, CPU) so that rank 0 reports the world it
+        # ran in; only rank 0 then times the oracle
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        t = torch.ones(1)
+        dist.all_reduce(t)
+        n_ranks = int(t.item())
+        dist.destroy_process_group()
     if rank != 0:
         return 0
     inp = workloads.make_inputs(w, seed=0)
@@ -238,25 +254,38 @@ def run_reference(args, w):
     dt = time.perf_counter() - t0
     value = n * args.steps / dt
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": n_ranks,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": config_of(w, extra={"sample_tokens": n}),
+        "data": "synthetic", "config": config_of(w),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": "first %d of %d tokens per step, single-threaded C oracle" % (n, w.N),
-                         "host": host_cpu()},
+                         "sample_tokens": n, "host": host_cpu()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
-def config_of(w, extra=None):
-    c = {"workload": w.describe(), "N": w.N, "E": w.E, "K": w.K, "R": w.R, "H": w.H,
-         "alignment": w.alignment, "parallelism": "replicas"}
-    if extra:
-        c.update(extra)
-    return c
+def touched_bytes(w, P: int) -> int:
+    """HBM bytes one step must touch at minimum (route + permute + combine)."""
+    ab = algorithmic_bytes(w, P)
+    return ab["route"] + ab["permute"] + ab["combine"]
+
+
+def flushes_l2(w) -> bool:
+    """Workloads touching less than twice the L2 (with the fewest rows a plan
+    can have, P = N*K) flush it before every timed step."""
+    return touched_bytes(w, w.N * w.K) < 2 * L2_BYTES
+
+
+def config_of(w):
+    """The workload, identical in both arms (the driver compares the two)."""
+    l2 = ("L2 flushed (256 MB memset) before each timed step, steps timed one by one"
+          if flushes_l2(w) else
+          "inputs larger than L2 (at least %.0f MB touched per step)" % (touched_bytes(w, w.N * w.K) / 1e6))
+    return {"workload": w.describe(), "N": w.N, "E": w.E, "K": w.K, "R": w.R, "H": w.H,
+            "alignment": w.alignment, "parallelism": "replicas", "l2": l2}
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -349,8 +378,8 @@ def run_ours(args, w):
 
     # inputs smaller than twice the 129 MB L2: flush it (a 256 MB memset)
     # before every timed step and time the steps one by one
-    touched = sum(algorithmic_bytes(w, P)[k] for k in ("route", "permute", "combine"))
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if touched < 2 * L2_BYTES else None
+    touched = touched_bytes(w, P)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flushes_l2(w) else None
 
     def timed_steps(k):
         """Exactly k steps: k // 10 replays of the 10-step graph, k % 10 of the 1-step one."""
@@ -466,24 +495,29 @@ def run_ours(args, w):
                    "gbs": round((ab[k] if k in ab else ab["plan_count"] + ab["plan_scatter"])
                                 / (stage_ms[k] * 1e-3) / 1e9, 1)}
                for k in stage_ms}
+    rp_ms = stage_ms["route"] + stage_ms["plan"]
+    rp_bytes = ab["route"] + ab["plan_count"] + ab["plan_scatter"]
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_of(w, extra={"P": P, "l2": ("inputs larger than L2 (%.0f MB touched per step)"
-                                                     % (touched / 1e6)) if flush is None else
-                                      ("L2 flushed (256 MB memset) before each timed step, steps timed one by one; "
-                                       "%.1f MB touched per step" % (touched / 1e6)),
-                                      "experts": "identity (combine reads the permuted rows)",
-                                      "launch": "CUDA graphs of 10 steps (and of 1 step for K mod 10)"
-                                      if flush is None else "CUDA graph of one step per timed step",
-                                      "permute": "early_x: x row loads overlap the plan kernel"}),
+        "config": config_of(w),
+        "method": {"P": P, "touched_mb_per_step": round(touched / 1e6, 1),
+                   "experts": "identity (combine reads the permuted rows)",
+                   "launch": "CUDA graphs of 10 steps (and of 1 step for K mod 10)"
+                   if flush is None else "CUDA graph of one step per timed step",
+                   "permute": "early_x: x row loads overlap the plan kernel"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "traffic": committed_traffic(dom, w.name),
                      "algorithmic_bytes": ab[dom]},
         "kernels": kernels,
-        "route_plan_us": round(1e3 * (stage_ms["route"] + stage_ms["plan"]), 2),
+        "route_plan_us": round(1e3 * rp_ms, 2),
+        "route_plan": {"us": round(1e3 * rp_ms, 2), "algorithmic_bytes": rp_bytes,
+                       "gbs": round(rp_bytes / (rp_ms * 1e-3) / 1e9, 1),
+                       "frac": round(rp_bytes / (rp_ms * 1e-3) / 1e9 / peak, 4),
+                       "launches": m.route_plan_launches(w.N, w.E, w.K, w.R, w.n_group),
+                       "how": "route and plan each timed alone (graphs of 10 back-to-back calls), summed"},
         "route_plan_launches": m.route_plan_launches(w.N, w.E, w.K, w.R, w.n_group),
         "cpu_baseline": cpu,
         "e2e": {"value": ws * w.N / (e2e_ms * 1e-3), "unit": "tokens/s",
@@ -566,19 +600,45 @@ def run_stage(args, w):
     return 0
 
 
-def main(argv=None):
+def launch_ranks(n: int, argv) -> int:
+    """Start n ranks of this script on this node (torch.distributed.run,
+    rendezvous on 127.0.0.1) and return the launcher's exit code."""
+    import socket
+    sock = socket.socket()
+    sock.bind(("127.0.0.1", 0))
+    port = sock.getsockname()[1]
+    sock.close()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(n),
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + list(argv)
+    return subprocess.run(cmd).returncode
+
+
+def build_parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="mixtral", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--config", default="large", choices=sorted(workloads.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--stage", choices=["all", "route", "plan", "permute", "combine", "balanced", "tile_map",
                                         "rank_layout"], default="all",
                     help="time one step of the path alone (a profiling case, not a contract line)")
     ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count N")
+    return ap
+
+
+def main(argv=None):
+    ap = build_parser()
     args = ap.parse_args(argv)
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    if args.stage == "all":
+        if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+            return launch_ranks(args.gpus, sys.argv[1:] if argv is None else list(argv))
+        ws = dist_env()[0]
+        if ws != args.gpus:
+            ap.error("--gpus %d but WORLD_SIZE=%d: launch one rank per GPU" % (args.gpus, ws))
     w = workloads.get(args.config)
     if args.tokens > 0:
         import dataclasses

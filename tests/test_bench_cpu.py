@@ -66,8 +66,41 @@ def test_reference_arm_prints_contract_line():
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
 
 
-def test_reference_arm_nonzero_rank_exits_quietly():
-    env = dict(os.environ, RANK="1", WORLD_SIZE="2")
-    res = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--config", "tiny"], cwd=ROOT,
-                         capture_output=True, text=True, timeout=300, env=env)
-    assert res.returncode == 0 and res.stdout.strip() == ""
+def test_gpus_flag_launches_its_ranks():
+    """A plain `bench.py --gpus 2` (no WORLD_SIZE) starts two ranks itself;
+    they meet over gloo, rank 0 alone prints the line and reports both."""
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_PORT")}
+    env["OMP_NUM_THREADS"] = "1"
+    res = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--config", "tiny", "--gpus", "2",
+                          "--steps", "1", "--warmup", "0"], cwd=ROOT, capture_output=True, text=True, timeout=600,
+                         env=env)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+
+
+def test_gpus_flag_must_match_the_launched_world():
+    env = dict(os.environ, RANK="0", WORLD_SIZE="2")
+    res = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--config", "tiny", "--gpus", "1"],
+                         cwd=ROOT, capture_output=True, text=True, timeout=300, env=env)
+    assert res.returncode != 0 and "WORLD_SIZE=2" in res.stderr
+
+
+def test_both_arms_describe_the_workload_with_the_same_config():
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+    for name in workloads.CONFIGS:
+        w = workloads.get(name)
+        c = bench.config_of(w)
+        assert c["workload"].startswith(name + ": N=%d E=%d K=%d R=%d H=%d" % (w.N, w.E, w.K, w.R, w.H))
+        assert ("flushed" in c["l2"]) == (name == "tiny")
+
+
+def test_default_workload_is_the_large_one():
+    sys.path.insert(0, ROOT)
+    import bench
+    args = bench.build_parser().parse_args([])
+    assert args.config == "large" and args.gpus == 1 and args.impl == "ours"
