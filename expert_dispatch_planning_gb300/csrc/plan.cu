@@ -2324,7 +2324,7 @@ extern "C" MOE_API int moe_route_plan(const float* logits, const float* bias, in
 // module, so the call needs no caller workspace and allocates nothing.
 // Every GPU that loads the library holds these bytes until the process
 // exits.  Host code must not use the symbol itself as a device address; the
-// address comes from cudaGetSymbolAddress once per device.
+// address comes from cudaGetSymbolAddress with the device current.
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // 1 MiB
@@ -2334,20 +2334,23 @@ constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device.  The first call
-// on a device looks the address up and zeroes the array on `stream` (the
+// Device address of the scratch array on the current device, looked up on
+// every call: a device reset (or a torn-down primary context) reloads the
+// module, and the array may then sit at a new address with unknown contents.
+// Whenever the address differs from the one last seen on this device (the
+// first call included), the array is zeroed on `stream` before use (the
 // plan's call counter and look-back flags start from zero).
 int scratch_for_current_device(cudaStream_t stream, void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_plan_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_plan_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+    if (g_scratch_ptr[dev] != p) {
         if (cudaMemsetAsync(p, 0, kNoAllocScratchBytes, stream) != cudaSuccess) return MOE_ERR_CUDA;
         g_scratch_ptr[dev] = p;
     }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return MOE_OK;
 }
 

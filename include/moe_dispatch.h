@@ -230,10 +230,12 @@ MOE_API int moe_plan(const int32_t* topk_idx, int N, int E, int K, int R, int al
  * under 0.6 MiB.  The call allocates nothing and runs the same kernels as
  * moe_plan, so its outputs are identical.
  *
- * The first call on each device looks up the array's device address and
- * zeroes it with a memset enqueued on `stream`; make that first call before
- * any stream capture.  All calls on a device share the one array and it keeps
- * the previous call's state, so calls that may overlap on the GPU (different
+ * Every call looks up the array's device address on the current device.
+ * The first call on a device, and any call that finds the array at a new
+ * address (after a device reset reloaded the library's module), zeroes it
+ * with a memset enqueued on `stream`: make the first call on each device
+ * before any stream capture.  All calls on a device share the one array and
+ * it keeps the previous call's state, so calls that may overlap on the GPU (different
  * streams without ordering between them) race and give wrong plans: order
  * them on one stream or use moe_plan with separate workspaces.
  */

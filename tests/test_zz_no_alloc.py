@@ -1,12 +1,13 @@
-"""moe_plan_no_alloc against moe_plan, through the C ABI.
+"""moe_plan_no_alloc against the oracle and against moe_plan, through the C ABI.
 
 The no-allocation entry point serves callers that cannot allocate device
 memory (a host framework owns every buffer, or cudaMalloc's device-wide
 synchronisation is not acceptable): its scratch is a fixed array inside the
-library.  Its plan must equal the one moe_plan builds with a caller
-workspace, on consecutive calls that share that array.  This file is
-collected last so that a stop-at-first-failure run has already run every
-other test; it also passes on its own in a fresh process.
+library.  Its plan must equal the oracle's plan and the one moe_plan builds
+with a caller workspace, on consecutive calls of different sizes and plan
+paths that all share that array.  This file is collected last so that a
+stop-at-first-failure run has already run every other test; it also passes
+on its own in a fresh process.
 """
 import ctypes
 
@@ -14,6 +15,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -46,17 +48,52 @@ def _same(a, b):
         assert np.array_equal(np.asarray(ha[k]), np.asarray(hb[k])), k
 
 
-@pytest.mark.parametrize("name", ["qwen3", "large"])
-def test_no_alloc_matches_workspace_plan_on_consecutive_calls(m, name):
+def _same_as_oracle(p, topk, E, R, a):
+    got, want = p.to_host(), oracle.plan(topk, E, R, a)
+    for k in FIELDS + ["dup_groups", "dup_loffs"]:
+        assert np.array_equal(np.asarray(got[k]), np.asarray(want[k])), k
+
+
+def _check(m, w_or_shape, rng, path=None, monkeypatch=None):
+    N, E, K, R, a = w_or_shape
+    if path is not None:
+        monkeypatch.setenv("MOE_PLAN_PATH", path)
+    topk_np = workloads.random_topk(rng, N, E, K)
+    topk = torch.from_numpy(topk_np).to("cuda")
+    ref = m.plan(topk, E, R, a)
+    got = m.Plan.allocate(N, E, K, R, a)
+    _call_no_alloc(m, topk, got)
+    assert m.get_status(got) == 0 and m.get_status(ref) == 0
+    _same_as_oracle(got, topk_np, E, R, a)
+    _same(got, ref)
+    if path is not None:
+        monkeypatch.delenv("MOE_PLAN_PATH")
+
+
+def _shape(name):
     w = workloads.get(name)
+    return (w.N, w.E, w.K, w.R, w.alignment)
+
+
+@pytest.mark.parametrize("name", ["qwen3", "large"])
+def test_no_alloc_matches_oracle_and_workspace_plan_on_consecutive_calls(m, name):
     rng = np.random.default_rng(11)
-    for call in range(2):
-        topk = torch.from_numpy(workloads.random_topk(rng, w.N, w.E, w.K)).to("cuda")
-        ref = m.plan(topk, w.E, w.R, w.alignment)
-        got = m.Plan.allocate(w.N, w.E, w.K, w.R, w.alignment)
-        _call_no_alloc(m, topk, got)
-        assert m.get_status(got) == 0 and m.get_status(ref) == 0
-        _same(got, ref)
+    for _ in range(2):
+        _check(m, _shape(name), rng)
+
+
+def test_no_alloc_across_sizes_and_paths_sharing_the_array(m, monkeypatch):
+    """One process, one shared array: the large look-back plan, smaller plans
+    on the look-back and grid paths (the array's flags and counters left by
+    a bigger call), then the large plan again."""
+    rng = np.random.default_rng(12)
+    large = _shape("large")
+    _check(m, large, rng)
+    _check(m, (20000, 64, 8, 8, 16), rng, "lookback", monkeypatch)
+    _check(m, (4096, 256, 8, 64, 128), rng, "grid", monkeypatch)
+    _check(m, (777, 16, 3, 4, 8), rng, "lookback", monkeypatch)
+    _check(m, (8192, 128, 8, 8, 128), rng)          # the medium-E cluster kernel (no scratch)
+    _check(m, large, rng)
 
 
 def test_no_alloc_rejects_sizes_beyond_its_scratch(m):
