@@ -6,6 +6,7 @@
 // route_fast_kernel (route_fast.cuh): E = 32 G, sigmoid over groups of 32
 // experts or renormalised softmax, selection by approximate keys proved
 // exact, the exact router as the per-token fallback; bit-identical output.
+#include <algorithm>
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
@@ -131,7 +132,7 @@ int launch_route_fast(const RouteArgs& a, cudaStream_t stream) {
     constexpr int tokens_per_block = moe::RF_WARPS * (32 / G);
     const int64_t batches = (static_cast<int64_t>(a.N) + tokens_per_block - 1) / tokens_per_block;
     const size_t smem = sizeof(float) * (32 * G + moe::RF_WARPS * 1024);
-    // one wave of resident blocks, the same number of batches for every block
+    // a wave of resident blocks, the same number of batches for every block
     static std::atomic<int> per_sm_cache{0};  // the same for every GB300; 0: not queried yet
     int per_sm = per_sm_cache.load(std::memory_order_relaxed);
     if (per_sm == 0) {
@@ -142,7 +143,10 @@ int launch_route_fast(const RouteArgs& a, cudaStream_t stream) {
         per_sm_cache.store(per_sm, std::memory_order_relaxed);
     }
     const int64_t cap = static_cast<int64_t>(moe_host::num_sms()) * per_sm;
-    const int64_t rounds = (batches + cap - 1) / cap;
+    // one wave, or several when a block would get more tokens than its
+    // queue for the exact router holds
+    int64_t rounds = (batches + cap - 1) / cap;
+    rounds = std::min<int64_t>(rounds, moe::RF_DEFER / tokens_per_block);
     const int64_t blocks = (batches + rounds - 1) / rounds;
     // in stream order: started early, its blocks (17 KB of shared memory
     // each) slowed the kernel before it by more than the launch gap it hides

@@ -14,7 +14,8 @@
 //      fp32 input by moe_debug_route_sigmoid_error) plus one key rounding of
 //      the exact key.  The expert's lane-local index is packed into the 5
 //      low bits of a, so that packed keys are distinct within a lane; a
-//      6-deep min/max network keeps the lane's six largest.
+//      7-deep min/max network keeps the lane's seven largest (its first
+//      level propagates NaN, which marks a NaN logit).
 //   2. Group score = sum of the lane's two largest packed keys; the
 //      topk_group best groups (rank by shuffles within the token) are kept.
 //   3. K + 1 rounds of arg-max over the kept lanes' list heads (max by xor
@@ -29,11 +30,16 @@
 //      to the lower index.  The weights are computed in sorted position with
 //      the exact router's arithmetic and summation order, so the output is
 //      bit-identical to it.
-//   5. A token that fails a check (a margin, a lane that ran out of its six
-//      candidates, a NaN or infinite logit) is routed by the whole warp with
-//      the exact router's route_token; so is every token when a bias is not
-//      finite or exceeds 2^20 in magnitude.  The margins scale with the
-//      largest |bias| (the keys' ulp).
+//   5. A token that fails a check (a margin, a lane that ran out of its
+//      seven candidates, a NaN logit; with softmax scores any non-finite
+//      one) is routed by a whole warp with the exact router's route_token;
+//      so is every token when a bias is not finite or exceeds 2^20 in
+//      magnitude.  Such tokens are queued in shared memory and routed at the
+//      end of the block, their logits read again from global memory, so
+//      that no warp holds its batch loop on a slow token.  The margins scale
+//      with the largest |bias| (the keys' ulp).  An infinite logit needs no
+//      exception with sigmoid scores: its approximate key is within the
+//      bound like any other (the sweep covers every non-NaN input).
 //   Softmax: the key is the logit, so a packed key is within 2^-18 of it
 //   (relative); the margins are relative too, and out-of-order winners (a
 //   near-tie inside the top K) go to the exact router.  With 4 lanes per
@@ -90,9 +96,18 @@ __device__ __forceinline__ FastMargins fast_margins(float bmax) {
     m.g = __fmul_ru(2.125f, __fadd_ru(__fmul_ru(2.0f, eps), __fmul_ru(2.0f, u)));
     return m;
 }
-constexpr int RF_D = 6;        // candidates kept per lane
+constexpr int RF_D = 7;        // candidates kept per lane
+constexpr int RF_DEFER = 512;  // tokens a block may hand to the exact router: every token
+                               // of the block (the launch keeps blocks within this)
 constexpr int RF_THREADS = 128;
 constexpr int RF_WARPS = RF_THREADS / 32;
+
+// max that returns NaN when either input is NaN (fmaxf drops a NaN).
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
 
 __device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gmem_src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gmem_src)
@@ -129,11 +144,11 @@ __device__ __forceinline__ bool route_fast_token(const RouteArgs& a, const float
     const int K = a.K;
     const bool has_bias = a.bias != nullptr;
 
-    // ---- 1. packed approximate keys, the lane's six largest
+    // ---- 1. packed approximate keys, the lane's RF_D largest
     float L[RF_D];
 #pragma unroll
     for (int d = 0; d < RF_D; ++d) L[d] = -INFINITY;
-    float nan_chk = 0.0f;  // stays 0 unless a logit is NaN or infinite
+    float nan_chk = 0.0f;  // softmax: stays 0 unless a logit is NaN or infinite
     const float* grp = row + 32 * sub;
     const float* gb = s_bias + 32 * sub;
 #pragma unroll
@@ -152,22 +167,25 @@ __device__ __forceinline__ bool route_fast_token(const RouteArgs& a, const float
         const uint32_t jbase = 31u - 4u * static_cast<uint32_t>(c);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const float x = xs[u];
-            nan_chk = __fmaf_rn(x, 0.0f, nan_chk);
-            const float ak = SM ? x : __fadd_rn(sigmoid_approx(x), bs[u]);
-            float v = __uint_as_float((__float_as_uint(ak) & ~31u) | (jbase - static_cast<uint32_t>(u)));
+            // sigmoid: a NaN logit gives a NaN key (an infinite one a key
+            // within the bound); softmax keys are the logits, checked finite
+            if constexpr (SM) nan_chk = __fmaf_rn(xs[u], 0.0f, nan_chk);
+            const float ak = SM ? xs[u] : __fadd_rn(sigmoid_approx(xs[u]), bs[u]);
+            const float v = __uint_as_float((__float_as_uint(ak) & ~31u) | (jbase - static_cast<uint32_t>(u)));
+            // insertion into the sorted list: the new d-th largest is
+            // max(L[d], min(L[d-1], v)); a NaN stays in L[0] from then on
+            float n[RF_D];
+            n[0] = max_nan(L[0], v);
 #pragma unroll
-            for (int d = 0; d < RF_D; ++d) {
-                const float hi = fmaxf(L[d], v);
-                v = fminf(L[d], v);
-                L[d] = hi;
-            }
+            for (int d = 1; d < RF_D; ++d) n[d] = fmaxf(L[d], fminf(L[d - 1], v));
+#pragma unroll
+            for (int d = 0; d < RF_D; ++d) L[d] = n[d];
         }
     }
 
     // ---- 2. group selection (sigmoid)
     bool kept = true;
-    bool fail = !fast_ok || nan_chk != 0.0f;
+    bool fail = !fast_ok || L[0] != L[0] || nan_chk != 0.0f;
     if (!SM && a.n_group > 1 && a.topk_group < G) {
         const float S = __fadd_rn(L[0], L[1]);
         int rank = 0;
@@ -388,6 +406,13 @@ __global__ void __launch_bounds__(RF_THREADS, 8) route_fast_kernel(const RouteAr
     for (int w = 0; w < RF_WARPS; ++w) bmax = fmaxf(bmax, s_bmax[w]);
     const FastMargins mg = fast_margins(fast_ok ? bmax : 0.0f);
 
+    // tokens that failed a check, routed exactly after the batch loop (the
+    // launch gives a block at most RF_DEFER tokens, so the queue never fills)
+    __shared__ int32_t s_defer[RF_DEFER];
+    __shared__ int s_ndefer;
+    if (threadIdx.x == 0) s_ndefer = 0;
+    __syncthreads();
+
     for (; tok0 < a.N; tok0 += step) {
         float* cur = stage;
         cp_async_wait_0();
@@ -397,34 +422,44 @@ __global__ void __launch_bounds__(RF_THREADS, 8) route_fast_kernel(const RouteAr
         const float* row = cur + t * E;  // rows past N hold stale data; nothing is stored for them
         const bool fail = route_fast_token<G, SM>(a, row, s_bias, fast_ok, mg, sub, s, valid);
 
-        // tokens that failed a check: the exact router, the whole warp on one token
-        uint32_t pending = __ballot_sync(FULL_MASK, fail && valid && sub == 0);
-        while (pending != 0u) {
-            const int lt = __ffs(pending) - 1;  // lane t*G of the token
-            pending &= pending - 1u;
-            const int tt = lt / G;
-            const float* frow = cur + tt * E;
-            float raw[V], bias32[V];
-#pragma unroll
-            for (int j = 0; j < V / 4; ++j) {
-                const float4 q = *reinterpret_cast<const float4*>(frow + 4 * (lane + 32 * j));
-                raw[4 * j + 0] = q.x;
-                raw[4 * j + 1] = q.y;
-                raw[4 * j + 2] = q.z;
-                raw[4 * j + 3] = q.w;
-            }
-            lane_bias<32, V, true>(a, lane, bias32);
-            int my_idx[1];
-            float num[1];
-            route_token<32, V, true, 8>(a, raw, bias32, true, lane, lane, nullptr, my_idx, num);
-            if (lane < K) {
-                const int64_t st = tok0 + tt;
-                a.topk_idx[st * K + lane] = my_idx[0];
-                a.topk_w[st * K + lane] = num[0];
-            }
+        // tokens that failed a check: queued for the end of the block (N < 2^31)
+        const bool queue = fail && valid;
+        const uint32_t qmask = __ballot_sync(FULL_MASK, queue && sub == 0);
+        if (qmask != 0u) {
+            int base = 0;
+            if (lane == 0) base = atomicAdd(&s_ndefer, __popc(qmask));
+            base = __shfl_sync(FULL_MASK, base, 0);
+            const int slot = base + __popc(qmask & ((1u << lane) - 1u));
+            if (queue && sub == 0 && slot < RF_DEFER) s_defer[slot] = static_cast<int32_t>(s);
         }
         __syncwarp();  // every lane is done with the stage before it is refilled
         if (tok0 + step < a.N) issue(tok0 + step);
+    }
+
+    // the queued tokens, a warp each, by the exact router; their logits
+    // read again from global memory
+    __syncthreads();
+    const int nq = min(s_ndefer, RF_DEFER);
+    for (int i = warp; i < nq; i += RF_WARPS) {
+        const int64_t st = s_defer[i];
+        const float* lrow = a.logits + st * E;
+        float raw[V], bias32[V];
+#pragma unroll
+        for (int j = 0; j < V / 4; ++j) {
+            const float4 q = *reinterpret_cast<const float4*>(lrow + 4 * (lane + 32 * j));
+            raw[4 * j + 0] = q.x;
+            raw[4 * j + 1] = q.y;
+            raw[4 * j + 2] = q.z;
+            raw[4 * j + 3] = q.w;
+        }
+        lane_bias<32, V, true>(a, lane, bias32);
+        int my_idx[1];
+        float num[1];
+        route_token<32, V, true, 8>(a, raw, bias32, true, lane, lane, nullptr, my_idx, num);
+        if (lane < K) {
+            a.topk_idx[st * K + lane] = my_idx[0];
+            a.topk_w[st * K + lane] = num[0];
+        }
     }
 }
 

@@ -65,6 +65,7 @@ def adversarial_rows(rng, N, E, G):
     r4[:, 7] = r4[:, 5]                               # duplicate value at a likely boundary
     x[5::9, 3] = np.inf                               # non-finite logits
     x[6::9, 5] = -np.inf
+    x[0::97, 11] = np.nan
     x[7::9] *= 40.0                                   # sigmoid tails, tiny scores
     x[8::9] = -200.0 + rng.standard_normal((x[8::9].shape[0], E), dtype=np.float32)
     return x
@@ -107,6 +108,29 @@ def test_fast_with_unusable_bias_routes_every_token_exactly(m, monkeypatch, bias
     kw = dict(renormalize=True, n_group=8, topk_group=4, routed_scaling=1.0)
     fi, fw = route(m, x, 8, bias, monkeypatch, "auto", **kw)
     ei, ew = route(m, x, 8, bias, monkeypatch, "exact", **kw)
+    assert np.array_equal(fi, ei)
+    assert np.array_equal(fw.view(np.uint32), ew.view(np.uint32))
+
+
+@pytest.mark.parametrize("E,scoring", [(256, "sigmoid"), (128, "softmax")])
+def test_fast_every_token_failing_at_full_blocks(m, monkeypatch, E, scoring):
+    """Enough tokens that every block of the fast kernel holds the most
+    tokens its queue for the exact router takes, all of them failing a check
+    (an unusable bias; an infinite logit in every softmax row): the queued
+    tokens are routed exactly, identical to the exact kernel."""
+    rng = np.random.default_rng(E)
+    N = 700_000
+    x = rng.standard_normal((N, E), dtype=np.float32)
+    if scoring == "sigmoid":
+        bias = rng.uniform(-0.1, 0.1, E).astype(np.float32)
+        bias[5] = np.inf
+        kw = dict(renormalize=True, n_group=E // 32, topk_group=2, routed_scaling=2.5)
+    else:
+        bias = None
+        x[np.arange(N), rng.integers(0, E, N)] = -np.inf
+        kw = dict(renormalize=True, n_group=1, topk_group=1, routed_scaling=1.0)
+    fi, fw = route(m, x, 8 if scoring == "softmax" else 4, bias, monkeypatch, "auto", scoring=scoring, **kw)
+    ei, ew = route(m, x, 8 if scoring == "softmax" else 4, bias, monkeypatch, "exact", scoring=scoring, **kw)
     assert np.array_equal(fi, ei)
     assert np.array_equal(fw.view(np.uint32), ew.view(np.uint32))
 
