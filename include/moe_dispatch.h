@@ -112,7 +112,9 @@ MOE_API const char* moe_status_string(int code);
  * chosen top-K set and kept groups are separated from the rest by more
  * than twice the keys' error bound, evaluates the fixed sigmoid only for
  * the winners, and routes any token that fails a check (and every token
- * when a bias is not finite or exceeds 2^20) with the exact kernel.
+ * when a bias is not finite or exceeds 2^20) with the exact kernel's code,
+ * a warp per token after the block's other tokens (a block takes at most
+ * 512 tokens; very large N launches several waves of blocks).
  * MOE_ROUTE_PATH=exact in the environment keeps every call on the exact
  * kernel; MOE_ROUTE_PATH=fast takes the fast one at any token count.
  */
