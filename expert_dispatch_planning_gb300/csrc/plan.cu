@@ -1192,7 +1192,6 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_medium_kernel(const PlanArg
     __shared__ int32_t s_wr[PLAN_WARPS][SMALL_MAX + 1];
     __shared__ int32_t s_wg[PLAN_WARPS], s_wd[PLAN_WARPS];
     __shared__ int32_t s_gd[4];  // groups, duplicates of lower tiles; their totals
-    __shared__ int32_t s_P;
 
     cluster_arrive_relaxed();  // this CTA has started: the others may push into it once all have
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1296,6 +1295,15 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_medium_kernel(const PlanArg
     if (lane == 0) {
         s_wg[warp] = run_g;
         s_wd[warp] = run_d;
+    }
+    // -1 over this CTA's share of every row of src_of_slot; the pairs' rows
+    // are written after the cluster barrier below (release / acquire), so
+    // they land after these, and the padding and unused rows keep -1
+    {
+        const uint32_t cap = static_cast<uint32_t>(a.p_cap);  // < 2^31
+        const uint32_t share = (cap + ncta - 1u) / ncta;
+        const uint32_t b = share * crank, e = min(cap, b + share);
+        for (uint32_t j = b + tid; j < e; j += PLAN_THREADS) a.out.src_of_slot[j] = -1;
     }
     __syncthreads();
     cluster_wait();  // every CTA of the cluster has started
@@ -1432,14 +1440,12 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_medium_kernel(const PlanArg
             }
             c += pv[j];
         }
-        if (lane == 0) s_P = P;
         if (tile == 0 && lane == 0) {
             a.out.cu_seqlens[E] = P;
             a.out.rank_slot_offsets[R] = P;
         }
     }
     __syncthreads();
-    const int P = s_P;
 
     if (tile == 0 && warp == 1) {  // rank arrays (DeepEP notify_dispatch rank prefix)
         int tot_r = 0;
@@ -1505,22 +1511,6 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_medium_kernel(const PlanArg
     // neighbouring slots
     __syncthreads();
     for (int i = tid; i < s_tloc[E]; i += PLAN_THREADS) a.out.src_of_slot[s_gsl[i]] = s_src[i];
-
-    // ---- -1 into the padding rows (experts tile, tile + T, ...: a warp
-    // each) and into this tile's share of the unused rows [P, P_cap)
-    for (int e = tile + static_cast<int>(ncta) * warp; e < E; e += static_cast<int>(ncta) * PLAN_WARPS) {
-        const int cu = s_pad[e], tot = s_tot[e];
-        const int end = e + 1 < E ? s_pad[e + 1] : P;
-        for (int j = cu + tot + lane; j < end; j += 32)
-            if (j >= 0 && static_cast<int64_t>(j) < a.p_cap) a.out.src_of_slot[j] = -1;
-    }
-    {
-        const uint32_t cap = static_cast<uint32_t>(a.p_cap);  // < 2^31
-        const uint32_t rest = cap - static_cast<uint32_t>(P);
-        const uint32_t share = (rest + ncta - 1u) / ncta;
-        const uint32_t b = static_cast<uint32_t>(P) + share * crank, e = min(cap, b + share);
-        for (uint32_t j = b + tid; j < e; j += PLAN_THREADS) a.out.src_of_slot[j] = -1;
-    }
 }
 
 // ---------------------------------------------------------------- grid path
