@@ -78,3 +78,19 @@ def test_plan_at_the_workload(name):
         # the dedup-heavy shaping: most tokens send two or more pairs to one rank
         dst = np.asarray(p["dst"]).reshape(w.N, w.K)
         assert np.mean((dst < 0).any(axis=1)) > 0.5
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "qwen3"])
+def test_permute_at_the_workload(name):
+    """permuted[raw slot of pair f] = x[f // K]; padding rows +0; by numpy's
+    fancy indexing (the workloads whose buffers stay under a few hundred MB)."""
+    w = workloads.get(name)
+    inp = workloads.make_inputs(w, seed=0)
+    idx, _ = route(w, inp)
+    p = oracle.plan(idx, w.E, w.R, w.alignment)
+    dst = np.asarray(p["dst"], np.int64).ravel()
+    raw = np.where(dst >= 0, dst, -dst - 1)
+    want = np.zeros((p["P_cap"], w.H), np.uint16)
+    want[raw] = inp["x_bits"][np.arange(w.N * w.K) // w.K]
+    got = oracle.permute(inp["x_bits"], p["dst"], p["zero_fill_ranges"], w.K, p["P_cap"])
+    assert np.array_equal(got, want)
